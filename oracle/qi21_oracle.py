@@ -1,0 +1,374 @@
+"""CPU oracle of the Qwen-Image-2.1 single-stream DiT block (prefill + step).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module. The CUDA
+library never calls it, shares no code with it and has no fallback to it.
+
+Source: the docs.rs page of ``cortiq_engine/qwen_image21.rs`` (v0.8.4),
+the CPU-exact reference path. Each function names the item of that page it
+restates. Precision: everything in float64 (stricter than the page's f32
+activations and f32 host GEMM), except where the page fixes a float32 step
+that changes values beyond rounding: the RoPE tables (``rope_tables``: f32
+frequencies, f32 angle, f32 cos/sin). Matrix products use numpy's ``@``
+(a library primitive) with no blocking or reordering of the definition.
+
+Pinned by ``tests/test_oracle_pins.py`` (worked examples of the page's own
+tests, closed forms, brute force and invariants).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TEXT = 0
+IMAGE = 1
+
+
+# --------------------------------------------------------------- layout ----
+# qwen_image21.rs, "Seg", "Qi21Layout" (total, prefix_len, target, validate,
+# block_ids, positions).
+
+def seg_len(seg) -> int:
+    kind, a, b = seg
+    return a if kind == TEXT else a * b
+
+
+def total_rows(segs) -> int:
+    return sum(seg_len(s) for s in segs)
+
+
+def prefix_len(segs) -> int:
+    """Rows before the target block (the last segment)."""
+    return total_rows(segs) - seg_len(segs[-1])
+
+
+def validate(segs) -> None:
+    """The layout ends with a non-empty target image and has a non-empty
+    prefix (qwen_image21.rs, Qi21Layout::validate)."""
+    if not segs:
+        raise ValueError("empty layout")
+    kind, a, b = segs[-1]
+    if kind != IMAGE or a <= 0 or b <= 0:
+        raise ValueError("the layout must end with a non-empty target image block")
+    if prefix_len(segs) == 0:
+        raise ValueError("the prompt prefix is empty")
+
+
+def block_ids(segs) -> np.ndarray:
+    """Per row: -1 for text, else the running image-block id
+    (qwen_image21.rs, Qi21Layout::block_ids)."""
+    out = []
+    bid = 0
+    for kind, a, b in segs:
+        if kind == TEXT:
+            out += [-1] * a
+        else:
+            out += [bid] * (a * b)
+            bid += 1
+    return np.array(out, dtype=np.int32)
+
+
+def positions(segs) -> np.ndarray:
+    """(frame, h, w) RoPE positions of every row (qwen_image21.rs,
+    Qi21Layout::positions): a text row sits at [p, p, p] and advances p by
+    one; an image block of h x w rows holds the frame at p, centres row r on
+    r - (h - floor(h/2)) and column c on c - (w - floor(w/2)) in raster
+    order, then advances p by max(h, w)."""
+    out = []
+    p = 0
+    for kind, a, b in segs:
+        if kind == TEXT:
+            for _ in range(a):
+                out.append((p, p, p))
+                p += 1
+        else:
+            h, w = a, b
+            for r in range(h):
+                for c in range(w):
+                    out.append((p, r - (h - h // 2), c - (w - w // 2)))
+            p += max(h, w)
+    return np.array(out, dtype=np.int64).reshape(-1, 3)
+
+
+def prefix_visibility(segs) -> np.ndarray:
+    """Block-causal mask of the prefix as leading runs (qwen_image21.rs,
+    Qi21Dit::prefill): prefix row i sees keys [0, end[i]) with end[i] = i+1
+    for a text row and one past the last row of its own image block for an
+    image row."""
+    lp = prefix_len(segs)
+    ids = block_ids(segs)[:lp]
+    end = np.zeros(lp, dtype=np.uint32)
+    for i in range(lp):
+        if ids[i] < 0:
+            end[i] = i + 1
+        else:
+            e = i + 1
+            while e < lp and ids[e] == ids[i]:
+                e += 1
+            end[i] = e
+    return end
+
+
+def rope_tables(pos: np.ndarray, axes=(16, 56, 56), theta: float = 10000.0):
+    """cos/sin tables [rows, head_dim/2] in pair order frame, h, w
+    (qwen_image21.rs, rope_tables). The page fixes float32 here: the
+    frequency of pair i of an axis of width d is 1 / f32(theta)^(2i/d), the
+    angle is f32(position) * frequency, and cos/sin are taken in f32."""
+    pos = np.asarray(pos, dtype=np.int64).reshape(-1, 3)
+    freqs = []
+    for d in axes:
+        e = (2 * np.arange(d // 2, dtype=np.float32)) / np.float32(d)
+        freqs.append(np.float32(1.0) / np.power(np.float32(theta), e, dtype=np.float32))
+    cols = []
+    for a, fr in enumerate(freqs):
+        ang = pos[:, a].astype(np.float32)[:, None] * fr[None, :]
+        cols.append(ang.astype(np.float32))
+    ang = np.concatenate(cols, axis=1)
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def target_rope(segs, axes=(16, 56, 56), theta=10000.0):
+    """RoPE tables of the target rows at their positions after this
+    sequence's own prefix (qwen_image21.rs, Qi21Dit::target_rope)."""
+    pos = positions(segs)
+    return rope_tables(pos[prefix_len(segs):], axes, theta)
+
+
+# --------------------------------------------------------------- pieces ----
+
+def silu(v):
+    """v / (1 + e^-v) (qwen_image21.rs, silu)."""
+    return v / (1.0 + np.exp(-v))
+
+
+def layer_norm(x, eps):
+    """Affine-free LayerNorm with biased variance over the last axis
+    (qwen_image21.rs, layer_norm_into)."""
+    x = np.asarray(x, dtype=np.float64)
+    mean = x.mean(axis=-1, keepdims=True)
+    var = ((x - mean) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mean) / np.sqrt(var + eps)
+
+
+def norm_mod(x, scale, eps):
+    """dst = LN(x) * (1 + scale) (qwen_image21.rs, Qi21Dit::norm_mod)."""
+    return layer_norm(x, eps) * (1.0 + np.asarray(scale, dtype=np.float64))
+
+
+def gated_add(x, y, gate_raw):
+    """x + tanh(gate) * y (qwen_image21.rs, Qi21Dit::gated_add; the gate
+    chunk is tanh-ed first, as block_cpu does)."""
+    return x + np.tanh(np.asarray(gate_raw, dtype=np.float64)) * y
+
+
+def rms_norm(v, w, eps):
+    """Per-vector RMSNorm over the last axis times the weight as is
+    (qwen_image21.rs, rms_norm_inplace)."""
+    v = np.asarray(v, dtype=np.float64)
+    ss = (v * v).mean(axis=-1, keepdims=True)
+    return v / np.sqrt(ss + eps) * np.asarray(w, dtype=np.float64)
+
+
+def rope_rotate(v, cos, sin):
+    """Rotate the interleaved pairs (v[2j], v[2j+1]) of each head vector by
+    the row's angle j: (a c - b s, a s + b c) (qwen_image21.rs,
+    Qi21Dit::qk_norm_rope). v: [rows, heads, hd]; cos/sin: [rows, hd/2]."""
+    a = v[..., 0::2]
+    b = v[..., 1::2]
+    c = np.asarray(cos, dtype=np.float64)[:, None, :]
+    s = np.asarray(sin, dtype=np.float64)[:, None, :]
+    out = np.empty_like(v)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def qk_norm_rope(t, w, cos, sin, heads, head_dim, eps):
+    """Per (row, head): RMSNorm * w over head_dim, then the interleaved
+    RoPE (qwen_image21.rs, Qi21Dit::qk_norm_rope). t: [rows, heads*hd]."""
+    rows = t.shape[0]
+    v = np.asarray(t, dtype=np.float64).reshape(rows, heads, head_dim)
+    v = rms_norm(v, w, eps)
+    return rope_rotate(v, cos, sin).reshape(rows, heads * head_dim)
+
+
+def masked_softmax(scores, visible):
+    """Row softmax over the first visible[i] entries of row i, the rest
+    exactly 0 (qwen_image21.rs, softmax_prefix)."""
+    s = np.asarray(scores, dtype=np.float64)
+    m = s.shape[1]
+    keep = np.arange(m)[None, :] < np.asarray(visible, dtype=np.int64)[:, None]
+    s = np.where(keep, s, -np.inf)
+    mx = s.max(axis=1, keepdims=True)
+    p = np.where(keep, np.exp(s - mx), 0.0)
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def attention(q, k, v, visible, heads, head_dim):
+    """Per head: q * (1/sqrt(hd)), S = q k^T, masked softmax with query i
+    seeing keys [0, visible[i]), O = P v (qwen_image21.rs,
+    Qi21Dit::attention). q: [n, heads*hd]; k, v: [m, heads*hd]."""
+    n = q.shape[0]
+    m = k.shape[0]
+    qh = np.asarray(q, dtype=np.float64).reshape(n, heads, head_dim)
+    kh = np.asarray(k, dtype=np.float64).reshape(m, heads, head_dim)
+    vh = np.asarray(v, dtype=np.float64).reshape(m, heads, head_dim)
+    scale = 1.0 / np.sqrt(head_dim)
+    out = np.empty((n, heads, head_dim), dtype=np.float64)
+    for h in range(heads):
+        s = (qh[:, h, :] * scale) @ kh[:, h, :].T
+        p = masked_softmax(s, visible)
+        out[:, h, :] = p @ vh[:, h, :]
+    return out.reshape(n, heads * head_dim)
+
+
+# ---------------------------------------------------------------- block ----
+
+def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None):
+    """One block on the query rows of x (qwen_image21.rs, Qi21Dit::block_cpu):
+
+        xn = LN(x) (1 + s1); q, k, v = xn Wq^T, xn Wk^T, xn Wv^T
+        q, k <- qk RMSNorm + RoPE
+        o = attention(q, [k_prefix ++ k], [v_prefix ++ v], visible)
+        x += tanh(g1) (o Wo^T)
+        xn = LN(x) (1 + s2); x += tanh(g2) ((silu(xn Wg^T) * (xn Wu^T)) Wd^T)
+
+    x: [M, H]; W: dict of the layer's weights (float16 or float64 arrays);
+    mods: [4H] raw [s1|g1|s2|g2]; cos/sin: [M, hd/2] of the query rows;
+    kv_prefix: optional (K, V) [lp, H] post-RoPE keys/values seen first;
+    visible: [M] leading-run key counts (default: every key).
+
+    rows: optional subset of query rows whose output is wanted. Keys and
+    values are still formed from every row of x; the query-side work is
+    restricted to these rows (each output row depends only on its own
+    query and on all keys).
+
+    Returns (x_out [len(rows) or M, H], k [M, H], v [M, H]) with k, v the
+    block's own post-RoPE keys and values."""
+    H, nh, hd, eps = cfg["dim"], cfg["heads"], cfg["head_dim"], cfg["eps"]
+    f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    x = f(x)
+    mods = f(mods)
+    s1, g1, s2, g2 = mods[:H], mods[H:2 * H], mods[2 * H:3 * H], mods[3 * H:]
+    M = x.shape[0]
+    sel = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    xn = norm_mod(x, s1, eps)
+    k = qk_norm_rope(xn @ f(W["wk"]).T, W["norm_k"], cos, sin, nh, hd, eps)
+    v = xn @ f(W["wv"]).T
+    q = qk_norm_rope(xn[sel] @ f(W["wq"]).T, W["norm_q"], f(cos)[sel], f(sin)[sel], nh, hd, eps)
+    if kv_prefix is not None:
+        ka = np.concatenate([f(kv_prefix[0]), k], axis=0)
+        va = np.concatenate([f(kv_prefix[1]), v], axis=0)
+    else:
+        ka, va = k, v
+    if visible is None:
+        vis = np.full(len(sel), ka.shape[0], dtype=np.int64)
+    else:
+        vis = np.asarray(visible, dtype=np.int64)[sel]
+    o = attention(q, ka, va, vis, nh, hd)
+    xs = gated_add(x[sel], o @ f(W["wo"]).T, g1)
+    xn2 = norm_mod(xs, s2, eps)
+    hid = silu(xn2 @ f(W["wgate"]).T) * (xn2 @ f(W["wup"]).T)
+    xs = gated_add(xs, hid @ f(W["wdown"]).T, g2)
+    return xs, k, v
+
+
+def cfg_of(w) -> dict:
+    """Geometry dict of a synthetic workload."""
+    return {"dim": w.dim, "heads": w.heads, "head_dim": w.head_dim, "eps": w.eps,
+            "axes": tuple(w.axes), "theta": w.theta}
+
+
+def prefill(x_prefix, weights, mods0, segs, cfg, keep_x=False):
+    """The prefix through every block with the t = 0 modulation and the
+    block-causal mask, keeping each layer's own post-RoPE (K, V)
+    (qwen_image21.rs, Qi21Dit::prefill, host loop).
+
+    weights: list of per-layer weight dicts. Returns (cache, xs) with cache
+    a list of (K, V) [lp, H] per layer and xs the hidden state after each
+    block (if keep_x)."""
+    validate(segs)
+    lp = prefix_len(segs)
+    pos = positions(segs)
+    cos, sin = rope_tables(pos[:lp], cfg["axes"], cfg["theta"])
+    vis = prefix_visibility(segs)
+    x = np.asarray(x_prefix, dtype=np.float64)
+    cache, xs = [], []
+    for W in weights:
+        x, k, v = block(x, W, mods0, cos, sin, cfg, None, vis)
+        cache.append((k, v))
+        if keep_x:
+            xs.append(x)
+    return cache, xs
+
+
+def step(x_target, weights, mods, segs, cache, cfg, keep_x=False):
+    """The target rows through every block against [cached prefix, own rows]
+    with every key visible (qwen_image21.rs, Qi21Dit::step_cpu, the block
+    loop; the image embedding and the final projection are outside it).
+    Returns (x_out, xs)."""
+    validate(segs)
+    lp = prefix_len(segs)
+    x = np.asarray(x_target, dtype=np.float64)
+    n = x.shape[0]
+    cos, sin = target_rope(segs, cfg["axes"], cfg["theta"])
+    vis = np.full(n, lp + n, dtype=np.int64)
+    xs = []
+    for layer, W in enumerate(weights):
+        x, _, _ = block(x, W, mods, cos, sin, cfg, cache[layer], vis)
+        if keep_x:
+            xs.append(x)
+    return x, xs
+
+
+def joint_forward(x_prefix, x_target, weights, mods0, mods, segs, cfg):
+    """The whole joint sequence [prefix; target] through every block with
+    no cache: prefix rows modulated from t = 0 and target rows from t
+    (causal_condition), prefix row i seeing keys [0, end[i]) and target rows
+    seeing every key -- the block-causal mask of the page's module notes
+    ("(q >= kv) or same_image_block"). Returns the target rows' output.
+
+    The per-row modulation is a restatement, not a call of ``block``: each
+    row takes LN(x)(1+s) and the two gates of its own modulation set."""
+    validate(segs)
+    H, nh, hd, eps = cfg["dim"], cfg["heads"], cfg["head_dim"], cfg["eps"]
+    f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    lp = prefix_len(segs)
+    x = np.concatenate([f(x_prefix), f(x_target)], axis=0)
+    T = x.shape[0]
+    cos, sin = rope_tables(positions(segs), cfg["axes"], cfg["theta"])
+    vis = np.concatenate([prefix_visibility(segs).astype(np.int64), np.full(T - lp, T, dtype=np.int64)])
+    m = np.empty((T, 4 * H), dtype=np.float64)
+    m[:lp] = f(mods0)
+    m[lp:] = f(mods)
+    s1, g1, s2, g2 = m[:, :H], m[:, H:2 * H], m[:, 2 * H:3 * H], m[:, 3 * H:]
+    for W in weights:
+        xn = layer_norm(x, eps) * (1.0 + s1)
+        q = qk_norm_rope(xn @ f(W["wq"]).T, W["norm_q"], cos, sin, nh, hd, eps)
+        k = qk_norm_rope(xn @ f(W["wk"]).T, W["norm_k"], cos, sin, nh, hd, eps)
+        v = xn @ f(W["wv"]).T
+        o = attention(q, k, v, vis, nh, hd)
+        x = x + np.tanh(g1) * (o @ f(W["wo"]).T)
+        xn = layer_norm(x, eps) * (1.0 + s2)
+        hid = silu(xn @ f(W["wgate"]).T) * (xn @ f(W["wup"]).T)
+        x = x + np.tanh(g2) * (hid @ f(W["wdown"]).T)
+    return x[lp:]
+
+
+def mods_dev(mods, h):
+    """[s1 | tanh g1 | s2 | tanh g2]: the gate chunks tanh-ed in f32, the
+    scale chunks as they are (qi21.rs, mods_dev)."""
+    m = np.asarray(mods, dtype=np.float32)[:4 * h].copy()
+    m[h:2 * h] = np.tanh(m[h:2 * h])
+    m[3 * h:4 * h] = np.tanh(m[3 * h:4 * h])
+    return m
+
+
+# ------------------------------------------------------------- FLOP count --
+
+def step_flops(dim, mlp_hidden, layers, n_rows, visible_sum):
+    """Algorithmic work of one pass: GEMM flops 2 M (4 H^2 + 3 H I) per
+    layer plus attention 4 H sum_i visible(i) per layer (QK^T and PV over all
+    heads). Returns (gemm_flops, attn_flops)."""
+    g = 2.0 * n_rows * (4 * dim * dim + 3 * dim * mlp_hidden) * layers
+    a = 4.0 * dim * float(visible_sum) * layers
+    return g, a

@@ -1,0 +1,221 @@
+"""Seeded synthetic inputs for the Qwen-Image-2.1 single-stream block.
+
+This module holds no arithmetic of the method: it only names the workloads
+(their shapes, segment layouts and value distributions) and draws random
+tensors for them. Both the CPU oracle and the CUDA path consume what it
+returns; neither side imports the other.
+
+Recipe (one stream per tensor, so any single tensor can be rebuilt alone):
+
+* tensor ``(tag, index)`` of workload seed ``s`` is the concatenation of
+  chunks of ``CHUNK`` standard normals (float32, numpy ``PCG64`` seeded with
+  ``SeedSequence([s, TAG_ID[tag], index, chunk])``), multiplied in float32
+  by the tag's standard deviation, plus 1 for the RMSNorm weights;
+* hidden states ``x`` ~ N(0, 1) float32;
+* modulation vectors ``[scale1 | gate1 | scale2 | gate2]`` ~ N(0, 0.1)
+  float32, one set for the step (``mods_t``) and one for the t = 0 prefix
+  (``mods0``);
+* projection weights ~ N(0, fan_in^-1/2) (standard deviation), rounded to
+  float16 (round to nearest even) -- the oracle widens exactly these values;
+  fan_in = dim for q, k, v, o, gate, up and mlp_hidden for down;
+* per-head RMSNorm weights ``norm_q``, ``norm_k`` = 1 + N(0, 0.05) float32.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import dataclasses
+import os
+
+import numpy as np
+
+CHUNK = 1 << 22
+
+TAG_ID = {
+    "x_prefix": 1,
+    "x_target": 2,
+    "mods_t": 3,
+    "mods0": 4,
+    "wq": 10,
+    "wk": 11,
+    "wv": 12,
+    "wo": 13,
+    "wgate": 14,
+    "wup": 15,
+    "wdown": 16,
+    "norm_q": 17,
+    "norm_k": 18,
+}
+
+# Segment kinds, as the library's C ABI numbers them.
+TEXT = 0
+IMAGE = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: model geometry, the prompt prefix of each
+    sequence and the shared target image block."""
+
+    name: str
+    dim: int
+    heads: int
+    mlp_hidden: int
+    layers: int
+    prefixes: tuple  # per sequence: tuple of (kind, a, b) segments
+    target: tuple  # (h, w) of the target image block
+    head_dim: int = 128
+    axes: tuple = (16, 56, 56)
+    eps: float = 1e-6
+    theta: float = 10000.0
+    seed: int = 0
+
+    @property
+    def nseq(self) -> int:
+        return len(self.prefixes)
+
+    def segs(self, s: int = 0) -> list:
+        """Segment list of sequence ``s``: its prefix then the target."""
+        return list(self.prefixes[s]) + [(IMAGE, self.target[0], self.target[1])]
+
+    @property
+    def n_target(self) -> int:
+        return self.target[0] * self.target[1]
+
+    def prefix_rows(self, s: int = 0) -> int:
+        tot = 0
+        for kind, a, b in self.prefixes[s]:
+            tot += a if kind == TEXT else a * b
+        return tot
+
+
+def _t(n):
+    return (TEXT, n, 0)
+
+
+def _i(h, w):
+    return (IMAGE, h, w)
+
+
+WORKLOADS = {
+    # single block, dim 256 (2 heads), prefix Text(18), target Image(16,16)
+    "tiny_block_d256": Workload("tiny_block_d256", 256, 2, 768, 1, ((_t(18),),), (16, 16)),
+    # one full-width block, prefix Text(18), target Image(64,64)
+    "block_d4096_n4096": Workload("block_d4096_n4096", 4096, 32, 12288, 1, ((_t(18),),), (64, 64)),
+    # 32 blocks, prefix Text(18) + condition Image(64,64), target Image(64,64)
+    "step32_cond4114_n4096": Workload(
+        "step32_cond4114_n4096", 4096, 32, 12288, 32, ((_t(18), _i(64, 64)),), (64, 64)
+    ),
+    # 32 blocks, prefix Text(18), target Image(128,128)
+    "step32_n16384": Workload("step32_n16384", 4096, 32, 12288, 32, ((_t(18),),), (128, 128)),
+    # CFG pair: prefixes Text(18) and Text(1), shared target Image(32,32)
+    "cfg_pair32_n1024": Workload(
+        "cfg_pair32_n1024", 4096, 32, 12288, 32, ((_t(18),), (_t(1),)), (32, 32)
+    ),
+    # --- extra parity cases (small, several tiles, ragged tails) ---
+    # 32 chained blocks at dim 256 with a mixed block-causal prefix
+    "chain32_d256_mixed": Workload(
+        "chain32_d256_mixed", 256, 2, 768, 32, ((_t(5), _i(4, 6), _t(3), _i(3, 2)),), (10, 13)
+    ),
+    # ragged: 130 target rows, 150-row prefix with a 12x11 image block
+    "ragged_d512": Workload("ragged_d512", 512, 4, 1536, 2, ((_t(7), _i(12, 11), _t(11)),), (10, 13)),
+    # CFG pair at dim 256, prefixes of different lengths
+    "cfg_pair_d256": Workload("cfg_pair_d256", 256, 2, 768, 2, ((_t(18),), (_t(1),)), (9, 15)),
+    # smallest target: one row, one-row prefix
+    "single_row_d256": Workload("single_row_d256", 256, 2, 768, 1, ((_t(1),),), (1, 1)),
+}
+
+
+def _stream_chunk(seed: int, tag: str, index: int, chunk: int, count: int) -> np.ndarray:
+    ss = np.random.SeedSequence([seed, TAG_ID[tag], index, chunk])
+    return np.random.Generator(np.random.PCG64(ss)).standard_normal(count, dtype=np.float32)
+
+
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = _cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
+
+
+def normal(seed: int, tag: str, index: int, count: int, std: float, out: np.ndarray | None = None,
+           dtype=np.float32, offset: float = 0.0) -> np.ndarray:
+    """``count`` draws of tensor (tag, index): f32 standard normals times
+    f32(std), plus ``offset``, cast to ``dtype`` (into ``out`` if given)."""
+    if out is None:
+        out = np.empty(count, dtype=dtype)
+    assert out.size == count and out.dtype == np.dtype(dtype)
+    std32 = np.float32(std)
+    off32 = np.float32(offset)
+    nchunks = (count + CHUNK - 1) // CHUNK
+
+    def one(c):
+        lo = c * CHUNK
+        hi = min(count, lo + CHUNK)
+        z = _stream_chunk(seed, tag, index, c, hi - lo)
+        z *= std32
+        if offset != 0.0:
+            z += off32
+        out[lo:hi] = z.astype(dtype, copy=False)
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            one(c)
+    else:
+        list(_pool().map(one, range(nchunks)))
+    return out
+
+
+def x_prefix(w: Workload, s: int = 0) -> np.ndarray:
+    """Prefix hidden states of sequence ``s``: float32 [lp, dim], N(0, 1)."""
+    lp = w.prefix_rows(s)
+    return normal(w.seed, "x_prefix", s, lp * w.dim, 1.0).reshape(lp, w.dim)
+
+
+def x_target(w: Workload) -> np.ndarray:
+    """Target hidden states, shared by every sequence: float32 [n, dim]."""
+    return normal(w.seed, "x_target", 0, w.n_target * w.dim, 1.0).reshape(w.n_target, w.dim)
+
+
+def mods_t(w: Workload) -> np.ndarray:
+    """Step modulation [scale1|gate1|scale2|gate2]: float32 [4·dim], N(0, 0.1)."""
+    return normal(w.seed, "mods_t", 0, 4 * w.dim, 0.1)
+
+
+def mods0(w: Workload) -> np.ndarray:
+    """t = 0 modulation of the prefix: float32 [4·dim], N(0, 0.1)."""
+    return normal(w.seed, "mods0", 0, 4 * w.dim, 0.1)
+
+
+WEIGHT_TAGS = ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown")
+
+
+def weight_shape(w: Workload, tag: str) -> tuple:
+    H, I = w.dim, w.mlp_hidden
+    return {
+        "wq": (H, H), "wk": (H, H), "wv": (H, H), "wo": (H, H),
+        "wgate": (I, H), "wup": (I, H), "wdown": (H, I),
+    }[tag]
+
+
+def weight(w: Workload, layer: int, tag: str, out: np.ndarray | None = None) -> np.ndarray:
+    """Projection weight of ``layer`` in nn.Linear layout [out, in], float16."""
+    rows, cols = weight_shape(w, tag)
+    flat = None if out is None else out.reshape(-1)
+    res = normal(w.seed, tag, layer, rows * cols, cols ** -0.5, out=flat, dtype=np.float16)
+    return res.reshape(rows, cols)
+
+
+def norm_weight(w: Workload, layer: int, tag: str) -> np.ndarray:
+    """Per-head RMSNorm weight ``norm_q``/``norm_k``: float32 [head_dim]."""
+    return normal(w.seed, tag, layer, w.head_dim, 0.05, offset=1.0)
+
+
+def layer_weights(w: Workload, layer: int) -> dict:
+    """All weights of one layer (float16 projections, float32 norms)."""
+    d = {t: weight(w, layer, t) for t in WEIGHT_TAGS}
+    d["norm_q"] = norm_weight(w, layer, "norm_q")
+    d["norm_k"] = norm_weight(w, layer, "norm_k")
+    return d
