@@ -1,0 +1,430 @@
+"""Denoiser-step benchmark: target rows/s and TFLOP/s of the 32-block step
+(dim 4096, 32 heads x 128, mlp 12288, f16 operands / f32 accumulation) of
+a 64x64 target image against a 4114-row prefix (Text(18) + condition
+Image(64,64)), on synthetic seeded inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on a sample
+
+One JSON line on rank 0. Multi-GPU: independent replicas (one process per
+GPU, launched by torch.distributed.run), no data-path collective; the
+barrier and the max-over-ranks time only frame the measurement.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "step32_cond4114_n4096"
+METRIC = "denoiser-step target rows/s & TFLOP/s (32 blocks, 1024² = 4096 rows) vs f16 peak"
+UNIT = "target rows/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=0,
+                   help="query rows of the CPU sample (0 = all target rows)")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------ accounting --
+
+def pass_flops(w, n_rows, vis_sum):
+    """(gemm, attention) flops of one pass over n_rows rows and all layers:
+    GEMM 2 M (3H^2 + H^2 + 2HI + HI), attention 4 H sum_i visible(i)."""
+    H, I, L = w.dim, w.mlp_hidden, w.layers
+    gemm = 2.0 * n_rows * (4 * H * H + 3 * H * I) * L
+    attn = 4.0 * H * float(vis_sum) * L
+    return gemm, attn
+
+
+def class_work(w, n_rows, vis_sum):
+    """Algorithmic work of ONE launch of each kernel class in a step:
+    (kind, amount) with kind 'flop' (tensor bound) or 'byte' (HBM bound)."""
+    H, I, M = w.dim, w.mlp_hidden, n_rows
+    return {
+        "qkv": ("flop", 2.0 * M * 3 * H * H),
+        "o": ("flop", 2.0 * M * H * H),
+        "gateup": ("flop", 2.0 * M * 2 * I * H),
+        "down": ("flop", 2.0 * M * H * I),
+        "attention": ("flop", 4.0 * H * float(vis_sum)),
+        # x f32 read + xn f16 write per row
+        "rowop": ("byte", float(M) * H * (4 + 2)),
+        # q, k f16 read + write, cos/sin f32 read
+        "qkrope": ("byte", float(M) * (2 * H * 2 * 2 + 2 * 64 * 4)),
+        "kvcopy": ("byte", float(M) * 2 * H * 2 * 2),
+        "misc": ("byte", 4.0 * H * 4 * 2),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                mx.append(float(f[2].split()[0]))
+                power.append(float(f[3].split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val == "Active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------- CPU baseline --
+
+def oracle_layer_sample(w, r, reps=1):
+    """Time the oracle on layer 0 of the step: the keys/values of all n
+    target rows (against the layer-0 prefix cache) plus the query side of
+    the first r target rows, each part timed, scaled to n rows and L layers.
+    Returns (rows_per_s, seconds_measured, description)."""
+    import numpy as np
+
+    from oracle import qi21_oracle as O
+    from synthetic import qi21_inputs as S
+
+    cfg = O.cfg_of(w)
+    segs = w.segs(0)
+    lp = O.prefix_len(segs)
+    W = S.layer_weights(w, 0)
+    cp, sp = O.rope_tables(O.positions(segs)[:lp], cfg["axes"], cfg["theta"])
+    vis = O.prefix_visibility(segs)
+    # the layer-0 prefix cache (untimed): K/V of every prefix row
+    _, kp, vp = O.block(S.x_prefix(w, 0), W, S.mods0(w), cp, sp, cfg, None, vis, rows=[0])
+    ct, st = O.target_rope(segs, cfg["axes"], cfg["theta"])
+    x = S.x_target(w)
+    m = S.mods_t(w)
+    n = w.n_target
+    r = n if r <= 0 else min(r, n)
+    best = None
+    spent = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        O.block(x, W, m, ct, st, cfg, (kp, vp), None, rows=np.arange(r))
+        t1 = time.perf_counter()
+        t_all = t1 - t0
+        if r < n:
+            # the key/value side alone (query side restricted to one row)
+            O.block(x, W, m, ct, st, cfg, (kp, vp), None, rows=[0])
+            t2 = time.perf_counter()
+            t_kv = t2 - t1
+            t_layer = t_kv + (t_all - t_kv) * (n / r)
+            spent += t2 - t0
+        else:
+            t_layer = t_all
+            spent += t_all
+        best = t_layer if best is None else min(best, t_layer)
+    rows_per_s = n / (best * w.layers)
+    desc = (f"oracle (numpy float64, BLAS matmuls) on layer 0 of {w.layers}: K/V of all {n} target "
+            f"rows against the {lp}-row layer-0 cache + the query side of {r} of {n} rows; time "
+            f"scaled to {n} rows x {w.layers} layers")
+    return rows_per_s, spent, desc
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------ reference --
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synthetic import qi21_inputs as S
+    w = S.WORKLOADS[args.workload]
+    r = args.cpu_rows if args.cpu_rows > 0 else 128
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        rps, spent, desc = oracle_layer_sample(w, r)
+        if i >= args.warmup:
+            times.append(w.n_target / rps / w.layers)  # estimated seconds per layer
+    t_layer = statistics.median(times)
+    value = w.n_target / (t_layer * w.layers)
+    ms = t_layer * w.layers * 1e3
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w, n_gpus):
+    return {"workload": w.name, "dim": w.dim, "heads": w.heads, "head_dim": w.head_dim,
+            "mlp_hidden": w.mlp_hidden, "layers": w.layers,
+            "prefix_rows": [w.prefix_rows(s) for s in range(w.nseq)], "target_rows": w.n_target,
+            "sequences": w.nseq, "parallelism": f"replicas x{n_gpus}",
+            "l2": "inputs larger than L2: every step streams all 32 layers' weights (13.96 GB f16) "
+                  "and K/V caches"}
+
+
+# -------------------------------------------------------------- GPU arm --
+
+def run_gpu(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import diffusion_transformer_denoiser_qi21_gb300 as q
+    from diffusion_transformer_denoiser_qi21_gb300.make import build as make
+    from synthetic import device as D
+    from synthetic import qi21_inputs as S
+
+    make()
+    w = S.WORKLOADS[args.workload]
+    t0 = time.perf_counter()
+    dw = D.DeviceWorkload(w)
+    torch.cuda.synchronize()
+    t_setup = time.perf_counter() - t0
+    n_rows = w.nseq * w.n_target
+    lp = [c.lp for c in dw.caches]
+    vis_sum = sum(w.n_target * (lp_s + w.n_target) for lp_s in lp)
+    gemm_f, attn_f = pass_flops(w, n_rows, vis_sum)
+    flops_step = gemm_f + attn_f
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # prefill (once per prompt), timed on its own
+    dw.prefill_all()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(2):
+        dw.prefill_all()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1) / 2
+    if q.device_status() != 0:
+        raise RuntimeError("a kernel gave up waiting during the prefill")
+
+    for _ in range(args.warmup):
+        dw.step()
+    torch.cuda.synchronize()
+
+    gpu_index = local
+    vis_dev = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis_dev:
+        ids = [v.strip() for v in vis_dev.split(",") if v.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            gpu_index = int(ids[local])
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    _, launches0 = q.profile_read()
+    q.profile_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        dw.step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    class_ms, launches1 = q.profile_read()
+    q.profile_enable(False)
+    clk = clocks.stop()
+    if q.device_status() != 0:
+        raise RuntimeError("a kernel gave up waiting during the timed steps")
+    launches = {k: launches1[k] - launches0[k] for k in launches1}
+    gpu_launches = int(sum(launches.values()))
+
+    t_max = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    t_max_ms = float(t_max.item())
+    value = n_rows * args.steps * world / (t_max_ms * 1e-3)
+    tflops = flops_step * args.steps * world / (t_max_ms * 1e-3) / 1e12
+
+    # end to end through host buffers: pinned x in, x out back each step
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty_like(dw.x_target, device="cpu").pin_memory()
+        x_host.copy_(dw.x_target.cpu())
+        out_host = torch.empty_like(x_host).pin_memory()
+        m_host = dw.mods_t.cpu().pin_memory()
+        x_dev = torch.empty_like(dw.x_target)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            x_dev.copy_(x_host, non_blocking=True)
+            dw.mods_t.copy_(m_host, non_blocking=True)
+            dw.step(x_in=x_dev)
+            out_host.copy_(dw.x_out, non_blocking=True)
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device="cuda")
+        if dist is not None:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        h2d = x_host.numel() * 4 + m_host.numel() * 4
+        e2e = {"value": n_rows * args.steps * world / float(tt.item()), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_host.numel() * 4)}
+
+    peaks, peak_src = load_peaks()
+    work = class_work(w, n_rows, vis_sum)
+    classes = {}
+    total_cls = sum(class_ms.values()) or 1.0
+    for k, ms in class_ms.items():
+        nl = launches.get(k, 0)
+        if nl == 0 or ms <= 0:
+            continue
+        kind, amount = work[k]
+        per_launch_s = ms * 1e-3 / nl
+        if kind == "flop":
+            ach = amount / per_launch_s / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            unit = "TFLOP/s"
+        else:
+            ach = amount / per_launch_s / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        classes[k] = {"ms_per_step": ms / args.steps, "share": ms / total_cls, "launches": nl,
+                      "achieved": ach, "unit": unit, "frac": ach / peak}
+    dom = max(classes, key=lambda k: classes[k]["ms_per_step"])
+    dk = classes[dom]
+    kind, amount = work[dom]
+    roofline = {
+        "kernel": dom, "bound": "tensor" if kind == "flop" else "hbm", "achieved": dk["achieved"],
+        "peak": peaks["bf16_tflops_sustained"] if kind == "flop" else peaks["hbm_gbs"],
+        "unit": dk["unit"], "frac": dk["frac"], "traffic": None,
+        "peak_source": f"{peak_src}: " + ("bf16_tflops_sustained (f16 dense rate = bf16 dense rate)"
+                                          if kind == "flop" else "hbm_gbs"),
+        "algorithmic_per_launch": amount,
+    }
+    gemm_ms = sum(classes[k]["ms_per_step"] for k in ("qkv", "o", "gateup", "down") if k in classes)
+    attn_ms = classes.get("attention", {}).get("ms_per_step", 0.0)
+    fractions = {
+        "gemm_tflops": gemm_f / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
+        "attention_tflops": attn_f / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
+    }
+    fractions["gemm_frac"] = (fractions["gemm_tflops"] or 0) / peaks["bf16_tflops_sustained"]
+    fractions["attention_frac"] = (fractions["attention_tflops"] or 0) / peaks["bf16_tflops_sustained"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rps, spent, desc = oracle_layer_sample(w, args.cpu_rows)
+        cpu = {"value": rps, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+               "seconds": spent}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": _config(w, world), "tflops": tflops, "flops_per_step": flops_step,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+            "clocks": clk, "classes": classes, "fractions": fractions,
+            "prefill": {"ms": prefill_ms, "rows": lp, "rows_per_s": sum(lp) / (prefill_ms * 1e-3)},
+            "setup_s": t_setup,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) Qwen-Image-2.1 single-stream DiT block: prefill of the
+prompt prefix into a per-layer K/V cache and the denoiser step against it.
+
+Thin Python face of the C ABI in include/qi21.h (same names, argument
+marshalling only). Device buffers are torch CUDA tensors; streams are
+torch.cuda streams. There is no CPU fallback: the library must be built
+(``build()``) and a CUDA device present for any device call.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _binding as B
+from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_TEXT, Geom, Qi21Error,  # noqa: F401
+                       CLASSES, check, device_status, exported_symbols, profile_enable, profile_read, geom, layer_plane_bytes, layout_indices,
+                       layout_rows, load, workspace_bytes)
+
+__all__ = [
+    "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
+    "workspace_bytes", "pack_layer", "prefill", "step", "step_batch", "device_status", "build",
+    "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
+]
+
+
+def build(**kw) -> str:
+    from .make import build as _b
+    return _b(**kw)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (or None -> NULL)."""
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class PackedLayer:
+    """One block's packed device planes (keeps the plane buffer and the norm
+    weights alive) and the C struct pointing into them."""
+
+    def __init__(self, planes, norm_q, norm_k, cstruct):
+        self.planes = planes
+        self.norm_q = norm_q
+        self.norm_k = norm_k
+        self.c = cstruct
+
+
+def pack_layer(g: Geom, wq, wk, wv, wo, wgate, wup, wdown, norm_q, norm_k, stream=None) -> PackedLayer:
+    """qi21_pack_layer: f16 device weights in nn.Linear layout -> packed planes."""
+    torch = _torch()
+    lib = load()
+    nbytes = lib.qi21_layer_plane_bytes(C.byref(g))
+    if nbytes == 0:
+        check(lib.qi21_geom_check(C.byref(g)))
+    planes = torch.empty(nbytes, dtype=torch.uint8, device=wq.device)
+    out = B.Layer()
+    h = torch.float16
+    nq = norm_q.contiguous()
+    nk = norm_k.contiguous()
+    check(lib.qi21_pack_layer(C.byref(g), _ptr(wq, h, "wq"), _ptr(wk, h, "wk"), _ptr(wv, h, "wv"),
+                              _ptr(wo, h, "wo"), _ptr(wgate, h, "wgate"), _ptr(wup, h, "wup"),
+                              _ptr(wdown, h, "wdown"), _ptr(nq, torch.float32, "norm_q"),
+                              _ptr(nk, torch.float32, "norm_k"), planes.data_ptr(), nbytes, C.byref(out),
+                              _stream(stream)))
+    return PackedLayer(planes, nq, nk, out)
+
+
+def _layer_array(layers):
+    arr = (B.Layer * len(layers))()
+    for i, l in enumerate(layers):
+        arr[i] = l.c
+    return arr
+
+
+class KVCache:
+    """qi21_kvcache_alloc / qi21_kvcache_free: a per-prompt K/V cache owned
+    by the library."""
+
+    def __init__(self, g: Geom, segs):
+        self.g = g
+        self.segs = list(segs)
+        h = C.c_void_p()
+        check(load().qi21_kvcache_alloc(C.byref(g), B.segs_array(self.segs), len(self.segs), C.byref(h)))
+        self.handle = h
+        lp, n, L = C.c_int32(), C.c_int32(), C.c_int32()
+        check(load().qi21_kvcache_info(h, C.byref(lp), C.byref(n), C.byref(L)))
+        self.lp, self.n, self.layers = lp.value, n.value, L.value
+
+    def layer_ptr(self, layer: int) -> int:
+        p = C.c_void_p()
+        check(load().qi21_kvcache_layer(self.handle, layer, C.byref(p)))
+        return p.value
+
+    def layer_tensor(self, layer: int):
+        """A torch f16 [lp, 2H] copy of layer `layer`'s K|V (for checks)."""
+        return _device_view(self.layer_ptr(layer), (self.lp, 2 * self.g.dim), "<f2").clone()
+
+    def free(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            load().qi21_kvcache_free(self.handle)
+            self.handle = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+class _DevArray:
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _device_view(ptr: int, shape, typestr):
+    """A torch view of library-owned device memory (no copy)."""
+    torch = _torch()
+    return torch.as_tensor(_DevArray(ptr, shape, typestr), device="cuda")
+
+
+def prefill(g: Geom, layers, cache: KVCache, x_prefix, mods0, workspace, x_layers=None, stream=None):
+    """qi21_prefill."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_prefill(C.byref(g), _layer_array(layers), cache.handle, _ptr(x_prefix, f, "x_prefix"),
+                              _ptr(mods0, f, "mods0"), _ptr(x_layers, f, "x_layers"),
+                              _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                              _stream(stream)))
+
+
+def step(g: Geom, layers, cache: KVCache, x_in, x_out, mods, workspace, x_layers=None, stream=None):
+    """qi21_step."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_step(C.byref(g), _layer_array(layers), cache.handle, _ptr(x_in, f, "x_in"),
+                           _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _ptr(x_layers, f, "x_layers"),
+                           _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                           _stream(stream)))
+
+
+def step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace, x_layers=None, stream=None):
+    """qi21_step_batch (classifier-free-guidance batch of sequences)."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    check(load().qi21_step_batch(C.byref(g), _layer_array(layers), arr, len(caches), _ptr(x_in, f, "x_in"),
+                                 _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _ptr(x_layers, f, "x_layers"),
+                                 _ptr(workspace, None, "workspace"),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ------------------------------------------------------- single operations --
+
+def op_rowop(x, scale, xn=None, y=None, gate_t=None, eps=1e-6, stream=None):
+    torch = _torch()
+    rows, dim = x.shape
+    check(load().qi21_op_rowop(rows, dim, eps, _ptr(x, torch.float32, "x"), _ptr(y, torch.float32, "y"),
+                               _ptr(gate_t, torch.float32, "gate_t"), _ptr(scale, torch.float32, "scale"),
+                               _ptr(xn, torch.float16, "xn"), _stream(stream)))
+
+
+def op_mods_prep(mods, md, stream=None):
+    torch = _torch()
+    check(load().qi21_op_mods_prep(mods.numel() // 4, _ptr(mods, torch.float32, "mods"),
+                                   _ptr(md, torch.float32, "md"), _stream(stream)))
+
+
+def op_gemm(epi, A, Bw, out, gate_t=None, stream=None):
+    torch = _torch()
+    M, K = A.shape
+    N = Bw.shape[0]
+    check(load().qi21_op_gemm(epi, M, N, K, _ptr(A, torch.float16, "A"), _ptr(Bw, torch.float16, "B"),
+                              _ptr(out, None, "out"), out.shape[1], _ptr(gate_t, torch.float32, "gate_t"),
+                              _stream(stream)))
+
+
+def op_qkrope(panel, heads, norm_q, norm_k, cos_, sin_, eps=1e-6, stream=None):
+    torch = _torch()
+    check(load().qi21_op_qkrope(panel.shape[0], heads, eps, _ptr(panel, torch.float16, "panel"),
+                                _ptr(norm_q, torch.float32, "norm_q"), _ptr(norm_k, torch.float32, "norm_k"),
+                                _ptr(cos_, torch.float32, "cos"), _ptr(sin_, torch.float32, "sin"),
+                                _stream(stream)))
+
+
+def op_kvcopy(panel, kv, stream=None):
+    torch = _torch()
+    rows = panel.shape[0]
+    dim = panel.shape[1] // 3
+    check(load().qi21_op_kvcopy(rows, dim, _ptr(panel, torch.float16, "panel"), _ptr(kv, torch.float16, "kv"),
+                                _stream(stream)))
+
+
+def op_attention(panel, heads, out, nq, n_own, kv_pre=None, n_pre=0, vis=None, stream=None):
+    torch = _torch()
+    check(load().qi21_op_attention(nq, heads, _ptr(panel, torch.float16, "panel"),
+                                   _ptr(kv_pre, torch.float16, "kv_pre"), n_pre, n_own,
+                                   _ptr(vis, torch.int32, "vis"), _ptr(out, torch.float16, "out"),
+                                   _stream(stream)))

@@ -1,0 +1,778 @@
+// C ABI of the library (include/qi21.h): argument validation, the layout
+// index construction on the host, the per-prompt K/V cache object and the
+// launch sequences of the prefill and the step.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/qi21.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qi21 {
+
+static thread_local std::string t_err;
+
+static int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? QI21_ERR_OOM : QI21_ERR_CUDA, "%s: %s", what,
+              cudaGetErrorString(e));
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+unsigned int read_and_clear_status() {
+  cudaDeviceSynchronize();
+  return gemm_status_read_clear();
+}
+
+// ---------------------------------------------------------- profiling ----
+// Per-class device time: when enabled, every launch of a pass is bracketed
+// by two CUDA events recorded on the launch stream; qi21_profile_read sums
+// their elapsed times per class. Launches are counted whether or not the
+// events are on.
+
+struct ProfRec {
+  int cls;
+  cudaEvent_t a, b;
+};
+
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<cudaEvent_t> g_prof_pool;
+static std::vector<ProfRec> g_prof_recs;
+static size_t g_prof_used = 0;
+static std::atomic<long long> g_launches[QI21_NCLASS];
+
+static cudaEvent_t prof_event() {
+  if (g_prof_used == g_prof_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_prof_pool.push_back(e);
+  }
+  return g_prof_pool[g_prof_used++];
+}
+
+class ProfScope {
+ public:
+  ProfScope(int cls, cudaStream_t s) : cls_(cls), s_(s) {
+    g_launches[cls].fetch_add(1, std::memory_order_relaxed);
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    a_ = prof_event();
+    if (a_) cudaEventRecord(a_, s_);
+  }
+  ~ProfScope() {
+    if (!g_prof_on || a_ == nullptr) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEvent_t b = prof_event();
+    if (b == nullptr) return;
+    cudaEventRecord(b, s_);
+    g_prof_recs.push_back(ProfRec{cls_, a_, b});
+  }
+
+ private:
+  int cls_;
+  cudaStream_t s_;
+  cudaEvent_t a_ = nullptr;
+};
+
+// ------------------------------------------------------------- layout ----
+// qwen_image21.rs: Seg, Qi21Layout::{total, prefix_len, validate, block_ids,
+// positions}, rope_tables, and end[i] of Qi21Dit::prefill.
+
+struct Layout {
+  int total = 0, prefix = 0, target = 0;
+};
+
+static int layout_rows(const qi21_seg* segs, int nseg, Layout* out) {
+  if (segs == nullptr || nseg <= 0) return fail(QI21_ERR_ARG, "empty layout");
+  long long tot = 0;
+  for (int i = 0; i < nseg; ++i) {
+    const qi21_seg& s = segs[i];
+    if (s.kind == QI21_SEG_TEXT) {
+      if (s.a < 0) return fail(QI21_ERR_ARG, "segment %d: negative text length", i);
+      tot += s.a;
+    } else if (s.kind == QI21_SEG_IMAGE) {
+      if (s.a < 0 || s.b < 0) return fail(QI21_ERR_ARG, "segment %d: negative image side", i);
+      tot += static_cast<long long>(s.a) * s.b;
+    } else {
+      return fail(QI21_ERR_ARG, "segment %d: unknown kind %d", i, s.kind);
+    }
+    if (tot > (1LL << 30)) return fail(QI21_ERR_SHAPE, "layout too long");
+  }
+  const qi21_seg& last = segs[nseg - 1];
+  if (last.kind != QI21_SEG_IMAGE || last.a <= 0 || last.b <= 0)
+    return fail(QI21_ERR_SHAPE, "the layout must end with a non-empty target image block");
+  out->total = static_cast<int>(tot);
+  out->target = last.a * last.b;
+  out->prefix = out->total - out->target;
+  if (out->prefix == 0) return fail(QI21_ERR_SHAPE, "the prompt prefix is empty");
+  return QI21_OK;
+}
+
+static void layout_positions(const qi21_seg* segs, int nseg, std::vector<int64_t>& pos,
+                             std::vector<int32_t>& ids) {
+  pos.clear();
+  ids.clear();
+  int64_t p = 0;
+  int32_t bid = 0;
+  for (int i = 0; i < nseg; ++i) {
+    const qi21_seg& s = segs[i];
+    if (s.kind == QI21_SEG_TEXT) {
+      for (int r = 0; r < s.a; ++r) {
+        pos.push_back(p);
+        pos.push_back(p);
+        pos.push_back(p);
+        ids.push_back(-1);
+        ++p;
+      }
+    } else {
+      const int64_t h = s.a, w = s.b;
+      for (int64_t r = 0; r < h; ++r)
+        for (int64_t c = 0; c < w; ++c) {
+          pos.push_back(p);
+          pos.push_back(r - (h - h / 2));
+          pos.push_back(c - (w - w / 2));
+          ids.push_back(bid);
+        }
+      ++bid;
+      p += h > w ? h : w;
+    }
+  }
+}
+
+static void prefix_vis(const std::vector<int32_t>& ids, int lp, std::vector<uint32_t>& vis) {
+  vis.assign(lp, 0);
+  for (int i = 0; i < lp; ++i) {
+    if (ids[i] < 0) {
+      vis[i] = static_cast<uint32_t>(i + 1);
+    } else {
+      int e = i + 1;
+      while (e < lp && ids[e] == ids[i]) ++e;
+      vis[i] = static_cast<uint32_t>(e);
+    }
+  }
+}
+
+// f32 frequencies 1/theta^(2i/d), f32 angle = f32(pos) * freq, f32 cos/sin.
+static void rope_rows(const int64_t* pos, int rows, const int32_t axes[3], float theta, float* cs,
+                      float* sn) {
+  const int half = (axes[0] + axes[1] + axes[2]) / 2;
+  std::vector<float> freq;
+  std::vector<int> axis_of;
+  for (int a = 0; a < 3; ++a)
+    for (int i = 0; i < axes[a] / 2; ++i) {
+      const float e = static_cast<float>(2 * i) / static_cast<float>(axes[a]);
+      freq.push_back(1.0f / powf(theta, e));
+      axis_of.push_back(a);
+    }
+  for (int r = 0; r < rows; ++r)
+    for (int j = 0; j < half; ++j) {
+      const float ang = static_cast<float>(pos[3 * r + axis_of[j]]) * freq[j];
+      cs[static_cast<size_t>(r) * half + j] = cosf(ang);
+      sn[static_cast<size_t>(r) * half + j] = sinf(ang);
+    }
+}
+
+static int geom_check(const qi21_geom* g) {
+  if (g == nullptr) return fail(QI21_ERR_ARG, "null geometry");
+  if (g->head_dim != 128) return fail(QI21_ERR_GEOM, "head_dim %d (the kernels need 128)", g->head_dim);
+  if (g->heads <= 0 || g->heads * g->head_dim != g->dim)
+    return fail(QI21_ERR_GEOM, "heads*head_dim (%d*%d) != dim %d", g->heads, g->head_dim, g->dim);
+  if (g->dim % 128 != 0 || g->dim < 128 || g->dim > 8192)
+    return fail(QI21_ERR_GEOM, "dim %d (need a multiple of 128 in [128, 8192])", g->dim);
+  if (g->mlp_hidden <= 0 || g->mlp_hidden % 64 != 0)
+    return fail(QI21_ERR_GEOM, "mlp_hidden %d (need a positive multiple of 64)", g->mlp_hidden);
+  if (g->layers <= 0) return fail(QI21_ERR_GEOM, "layers %d", g->layers);
+  for (int a = 0; a < 3; ++a)
+    if (g->axes[a] < 0 || g->axes[a] % 2 != 0)
+      return fail(QI21_ERR_GEOM, "RoPE axis %d width %d must be even", a, g->axes[a]);
+  if (g->axes[0] + g->axes[1] + g->axes[2] != g->head_dim)
+    return fail(QI21_ERR_GEOM, "RoPE axes do not tile head_dim");
+  if (!(g->eps > 0.f) || !(g->theta > 0.f)) return fail(QI21_ERR_GEOM, "eps and theta must be > 0");
+  return QI21_OK;
+}
+
+// -------------------------------------------------------------- sizes ----
+
+static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t x, xn, panel, att, hid, md, total;
+};
+
+static WsLayout ws_layout(const qi21_geom* g, int rows) {
+  const size_t M = static_cast<size_t>(rows), H = g->dim, I = g->mlp_hidden;
+  WsLayout w{};
+  size_t off = 0;
+  w.x = off;
+  off = align256(off + M * H * 4);
+  w.xn = off;
+  off = align256(off + M * H * 2);
+  w.panel = off;
+  off = align256(off + M * 3 * H * 2);
+  w.att = off;
+  off = align256(off + M * H * 2);
+  w.hid = off;
+  off = align256(off + M * I * 2);
+  w.md = off;
+  off = align256(off + 4 * H * 4);
+  w.total = off;
+  return w;
+}
+
+}  // namespace qi21
+
+using namespace qi21;
+
+// ---------------------------------------------------------------- cache ----
+
+struct qi21_kvcache {
+  qi21_geom g;
+  std::vector<qi21_seg> segs;
+  int lp = 0, n = 0;
+  void* mem = nullptr;  // one allocation: kv, vis, tables
+  __half* kv = nullptr;  // [L][lp][2H]
+  uint32_t* vis = nullptr;
+  float* cos_p = nullptr;
+  float* sin_p = nullptr;
+  float* cos_t = nullptr;
+  float* sin_t = nullptr;
+  bool filled = false;
+};
+
+extern "C" {
+
+const char* qi21_last_error(void) { return t_err.c_str(); }
+
+const char* qi21_version(void) { return "qi21-gb300 0.1 (sm_103a)"; }
+
+int qi21_geom_check(const qi21_geom* g) { return geom_check(g); }
+
+int qi21_layout_rows(const qi21_seg* segs, int32_t nseg, int32_t* total, int32_t* prefix,
+                     int32_t* target) {
+  Layout L;
+  const int rc = layout_rows(segs, nseg, &L);
+  if (rc != QI21_OK) return rc;
+  if (total) *total = L.total;
+  if (prefix) *prefix = L.prefix;
+  if (target) *target = L.target;
+  return QI21_OK;
+}
+
+int qi21_layout_indices(const qi21_seg* segs, int32_t nseg, const int32_t axes[3], float theta,
+                        int64_t* pos, int32_t* block_ids, uint32_t* vis, float* cos_, float* sin_) {
+  Layout L;
+  int rc = layout_rows(segs, nseg, &L);
+  if (rc != QI21_OK) return rc;
+  if ((cos_ || sin_) && axes == nullptr) return fail(QI21_ERR_ARG, "null axes");
+  if (cos_ || sin_) {
+    for (int a = 0; a < 3; ++a)
+      if (axes[a] < 0 || axes[a] % 2) return fail(QI21_ERR_GEOM, "RoPE axis widths must be even");
+  }
+  std::vector<int64_t> p;
+  std::vector<int32_t> ids;
+  layout_positions(segs, nseg, p, ids);
+  if (pos) memcpy(pos, p.data(), p.size() * sizeof(int64_t));
+  if (block_ids) memcpy(block_ids, ids.data(), ids.size() * sizeof(int32_t));
+  if (vis) {
+    std::vector<uint32_t> v;
+    prefix_vis(ids, L.prefix, v);
+    memcpy(vis, v.data(), v.size() * sizeof(uint32_t));
+  }
+  if (cos_ || sin_) {
+    const int half = (axes[0] + axes[1] + axes[2]) / 2;
+    std::vector<float> c(static_cast<size_t>(L.total) * half), s(c.size());
+    rope_rows(p.data(), L.total, axes, theta, c.data(), s.data());
+    if (cos_) memcpy(cos_, c.data(), c.size() * sizeof(float));
+    if (sin_) memcpy(sin_, s.data(), s.size() * sizeof(float));
+  }
+  return QI21_OK;
+}
+
+size_t qi21_layer_plane_bytes(const qi21_geom* g) {
+  if (geom_check(g) != QI21_OK) return 0;
+  const size_t H = g->dim, I = g->mlp_hidden;
+  return align256(3 * H * H * 2) + align256(H * H * 2) + align256(2 * I * H * 2) + align256(H * I * 2);
+}
+
+size_t qi21_workspace_bytes(const qi21_geom* g, int32_t max_rows) {
+  if (geom_check(g) != QI21_OK || max_rows < 0) return 0;
+  return ws_layout(g, max_rows).total;
+}
+
+int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const void* wv,
+                    const void* wo, const void* wgate, const void* wup, const void* wdown,
+                    const float* norm_q, const float* norm_k, void* planes, size_t plane_bytes,
+                    qi21_layer* out, void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (!wq || !wk || !wv || !wo || !wgate || !wup || !wdown || !norm_q || !norm_k || !planes || !out)
+    return fail(QI21_ERR_ARG, "null pointer");
+  if (plane_bytes < qi21_layer_plane_bytes(g))
+    return fail(QI21_ERR_SHAPE, "plane buffer %zu bytes, need %zu", plane_bytes,
+                qi21_layer_plane_bytes(g));
+  if (reinterpret_cast<uintptr_t>(planes) % 256)
+    return fail(QI21_ERR_ARG, "planes must be 256-byte aligned");
+  const size_t H = g->dim, I = g->mlp_hidden;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(planes);
+  __half* wqkv = reinterpret_cast<__half*>(base);
+  __half* pwo = reinterpret_cast<__half*>(base + align256(3 * H * H * 2));
+  __half* w13 = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(pwo) + align256(H * H * 2));
+  __half* w2 = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(w13) + align256(2 * I * H * 2));
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(wqkv, wq, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(wqkv + H * H, wk, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(wqkv + 2 * H * H, wv, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(pwo, wo, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(w2, wdown, H * I * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "pack copies");
+  e = launch_pack_w13(static_cast<int>(I), static_cast<int>(H), static_cast<const __half*>(wgate),
+                      static_cast<const __half*>(wup), w13, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pack_w13");
+  out->wqkv = wqkv;
+  out->wo = pwo;
+  out->w13 = w13;
+  out->w2 = w2;
+  out->norm_q = norm_q;
+  out->norm_k = norm_k;
+  return QI21_OK;
+}
+
+int qi21_kvcache_alloc(const qi21_geom* g, const qi21_seg* segs, int32_t nseg, qi21_kvcache** out) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (out == nullptr) return fail(QI21_ERR_ARG, "null output");
+  *out = nullptr;
+  Layout L;
+  rc = layout_rows(segs, nseg, &L);
+  if (rc != QI21_OK) return rc;
+  std::vector<int64_t> p;
+  std::vector<int32_t> ids;
+  layout_positions(segs, nseg, p, ids);
+  std::vector<uint32_t> vis;
+  prefix_vis(ids, L.prefix, vis);
+  std::vector<float> c(static_cast<size_t>(L.total) * 64), s(c.size());
+  rope_rows(p.data(), L.total, g->axes, g->theta, c.data(), s.data());
+
+  const size_t H = g->dim;
+  const size_t kv_bytes = align256(static_cast<size_t>(g->layers) * L.prefix * 2 * H * 2);
+  const size_t vis_bytes = align256(static_cast<size_t>(L.prefix) * 4);
+  const size_t tp_bytes = align256(static_cast<size_t>(L.prefix) * 64 * 4);
+  const size_t tt_bytes = align256(static_cast<size_t>(L.target) * 64 * 4);
+  const size_t total = kv_bytes + vis_bytes + 2 * tp_bytes + 2 * tt_bytes;
+  auto* cc = new qi21_kvcache();
+  cc->g = *g;
+  cc->segs.assign(segs, segs + nseg);
+  cc->lp = L.prefix;
+  cc->n = L.target;
+  cudaError_t e = cudaMalloc(&cc->mem, total);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete cc;
+    return cuda_fail(e, "kv cache allocation");
+  }
+  uint8_t* b = static_cast<uint8_t*>(cc->mem);
+  cc->kv = reinterpret_cast<__half*>(b);
+  cc->vis = reinterpret_cast<uint32_t*>(b + kv_bytes);
+  cc->cos_p = reinterpret_cast<float*>(b + kv_bytes + vis_bytes);
+  cc->sin_p = reinterpret_cast<float*>(b + kv_bytes + vis_bytes + tp_bytes);
+  cc->cos_t = reinterpret_cast<float*>(b + kv_bytes + vis_bytes + 2 * tp_bytes);
+  cc->sin_t = reinterpret_cast<float*>(b + kv_bytes + vis_bytes + 2 * tp_bytes + tt_bytes);
+  const size_t lp64 = static_cast<size_t>(L.prefix) * 64;
+  if ((e = cudaMemcpy(cc->vis, vis.data(), L.prefix * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(cc->cos_p, c.data(), lp64 * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(cc->sin_p, s.data(), lp64 * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(cc->cos_t, c.data() + lp64, static_cast<size_t>(L.target) * 64 * 4,
+                      cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(cc->sin_t, s.data() + lp64, static_cast<size_t>(L.target) * 64 * 4,
+                      cudaMemcpyHostToDevice)) != cudaSuccess) {
+    cudaFree(cc->mem);
+    delete cc;
+    return cuda_fail(e, "kv cache tables");
+  }
+  *out = cc;
+  return QI21_OK;
+}
+
+void qi21_kvcache_free(qi21_kvcache* c) {
+  if (c == nullptr) return;
+  cudaDeviceSynchronize();
+  cudaFree(c->mem);
+  delete c;
+}
+
+int qi21_kvcache_info(const qi21_kvcache* c, int32_t* lp, int32_t* n, int32_t* layers) {
+  if (c == nullptr) return fail(QI21_ERR_ARG, "null cache");
+  if (lp) *lp = c->lp;
+  if (n) *n = c->n;
+  if (layers) *layers = c->g.layers;
+  return QI21_OK;
+}
+
+int qi21_kvcache_layer(const qi21_kvcache* c, int32_t layer, const void** kv) {
+  if (c == nullptr || kv == nullptr) return fail(QI21_ERR_ARG, "null pointer");
+  if (layer < 0 || layer >= c->g.layers) return fail(QI21_ERR_STATE, "layer %d out of range", layer);
+  *kv = c->kv + static_cast<size_t>(layer) * c->lp * 2 * c->g.dim;
+  return QI21_OK;
+}
+
+int qi21_device_status(void) { return static_cast<int>(read_and_clear_status()); }
+
+int qi21_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  g_prof_recs.clear();
+  g_prof_used = 0;
+  return QI21_OK;
+}
+
+int qi21_profile_read(float* ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (ms) {
+    for (int c = 0; c < QI21_NCLASS; ++c) ms[c] = 0.f;
+    for (const ProfRec& r : g_prof_recs) {
+      float t = 0.f;
+      if (cudaEventSynchronize(r.b) != cudaSuccess) return cuda_fail(cudaGetLastError(), "profile sync");
+      if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) ms[r.cls] += t;
+    }
+  }
+  if (launches)
+    for (int c = 0; c < QI21_NCLASS; ++c) launches[c] = g_launches[c].load(std::memory_order_relaxed);
+  g_prof_recs.clear();
+  g_prof_used = 0;
+  return QI21_OK;
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------- passes ----
+
+namespace {
+
+bool same_geom(const qi21_geom& a, const qi21_geom& b) {
+  return a.dim == b.dim && a.heads == b.heads && a.head_dim == b.head_dim &&
+         a.mlp_hidden == b.mlp_hidden && a.layers == b.layers && a.axes[0] == b.axes[0] &&
+         a.axes[1] == b.axes[1] && a.axes[2] == b.axes[2] && a.eps == b.eps && a.theta == b.theta;
+}
+
+int check_layers(const qi21_geom* g, const qi21_layer* layers) {
+  if (layers == nullptr) return fail(QI21_ERR_ARG, "null layers");
+  for (int l = 0; l < g->layers; ++l) {
+    const qi21_layer& w = layers[l];
+    if (!w.wqkv || !w.wo || !w.w13 || !w.w2 || !w.norm_q || !w.norm_k)
+      return fail(QI21_ERR_ARG, "layer %d: null plane", l);
+    if ((reinterpret_cast<uintptr_t>(w.wqkv) | reinterpret_cast<uintptr_t>(w.wo) |
+         reinterpret_cast<uintptr_t>(w.w13) | reinterpret_cast<uintptr_t>(w.w2)) % 16)
+      return fail(QI21_ERR_ARG, "layer %d: planes must be 16-byte aligned", l);
+  }
+  return QI21_OK;
+}
+
+#define QI21_CK(expr, what)                        \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// One layer's second half: attention -> O (+gate) -> LN2 -> gate/up -> down
+// (+gate); the first half (LN1, qkv, qkrope) is done by the caller.
+struct PassBufs {
+  float* x;
+  __half* xn;
+  __half* panel;
+  __half* att;
+  __half* hid;
+  float* md;
+};
+
+int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
+             qi21_kvcache* pcache, const qi21_kvcache* const* caches, int nseq, int n,
+             const PassBufs& b, float* x_layers, cudaStream_t s) {
+  const int H = g->dim, I = g->mlp_hidden, L = g->layers;
+  const float* s1 = b.md;
+  const float* g1 = b.md + H;
+  const float* s2 = b.md + 2 * H;
+  const float* g2 = b.md + 3 * H;
+
+  RopeTables tabs{};
+  if (prefill) {
+    tabs.nsrc = 1;
+    tabs.src[0] = RopeSrc{pcache->cos_p, pcache->sin_p, 0};
+  } else {
+    tabs.nsrc = nseq;
+    for (int q = 0; q < nseq; ++q) tabs.src[q] = RopeSrc{caches[q]->cos_t, caches[q]->sin_t, q * n};
+  }
+
+  {
+    ProfScope ps(QI21_CLASS_ROWOP, s);
+    QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s1, b.xn, s), "rowop");
+  }
+  for (int l = 0; l < L; ++l) {
+    const qi21_layer& w = layers[l];
+    const bool last = (l + 1 == L);
+    GemmPlan pq, po, p13, p2;
+    QI21_CK(make_gemm_plan(&pq, EPI_F16, M, 3 * H, H, b.xn, static_cast<const __half*>(w.wqkv),
+                           b.panel, 3 * H, nullptr),
+            "qkv plan");
+    {
+      ProfScope ps(QI21_CLASS_QKV, s);
+      QI21_CK(launch_gemm(pq, s), "qkv gemm");
+    }
+    {
+      ProfScope ps(QI21_CLASS_QKROPE, s);
+      QI21_CK(launch_qkrope(M, g->heads, g->eps, b.panel, w.norm_q, w.norm_k, tabs, s), "qkrope");
+    }
+    AttnArgs aa{};
+    aa.panel = b.panel;
+    aa.out = b.att;
+    aa.heads = g->heads;
+    if (prefill) {
+      __half* kv = pcache->kv + static_cast<size_t>(l) * pcache->lp * 2 * H;
+      {
+        ProfScope ps(QI21_CLASS_KVCOPY, s);
+        QI21_CK(launch_kvcopy(M, H, b.panel, kv, s), "kvcopy");
+      }
+      if (last) break;
+      aa.nseq = 1;
+      aa.seq[0] = AttnSeq{nullptr, 0, 0, M, 0, M, pcache->vis};
+    } else {
+      aa.nseq = nseq;
+      for (int q = 0; q < nseq; ++q) {
+        const qi21_kvcache* c = caches[q];
+        aa.seq[q] = AttnSeq{c->kv + static_cast<size_t>(l) * c->lp * 2 * H, c->lp, q * n, n, q * n, n,
+                            nullptr};
+      }
+    }
+    {
+      ProfScope ps(QI21_CLASS_ATTENTION, s);
+      QI21_CK(launch_attention(aa, s), "attention");
+    }
+    QI21_CK(make_gemm_plan(&po, EPI_RESID, M, H, H, b.att, static_cast<const __half*>(w.wo), b.x, H, g1),
+            "o plan");
+    {
+      ProfScope ps(QI21_CLASS_O, s);
+      QI21_CK(launch_gemm(po, s), "o gemm");
+    }
+    {
+      ProfScope ps(QI21_CLASS_ROWOP, s);
+      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s2, b.xn, s), "rowop");
+    }
+    QI21_CK(make_gemm_plan(&p13, EPI_SWIGLU, M, 2 * I, H, b.xn, static_cast<const __half*>(w.w13),
+                           b.hid, I, nullptr),
+            "w13 plan");
+    {
+      ProfScope ps(QI21_CLASS_GATEUP, s);
+      QI21_CK(launch_gemm(p13, s), "gate/up gemm");
+    }
+    QI21_CK(make_gemm_plan(&p2, EPI_RESID, M, H, I, b.hid, static_cast<const __half*>(w.w2), b.x, H, g2),
+            "down plan");
+    {
+      ProfScope ps(QI21_CLASS_DOWN, s);
+      QI21_CK(launch_gemm(p2, s), "down gemm");
+    }
+    if (x_layers)
+      QI21_CK(cudaMemcpyAsync(x_layers + static_cast<size_t>(l) * M * H, b.x,
+                              static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
+              "x_layers copy");
+    if (!last) {
+      ProfScope ps(QI21_CLASS_ROWOP, s);
+      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s1, b.xn, s), "rowop");
+    }
+  }
+  return QI21_OK;
+}
+
+int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b) {
+  if (ws == nullptr) return fail(QI21_ERR_WORKSPACE, "null workspace");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(QI21_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const WsLayout w = ws_layout(g, M);
+  if (ws_bytes < w.total) return fail(QI21_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, w.total);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  b->x = reinterpret_cast<float*>(base + w.x);
+  b->xn = reinterpret_cast<__half*>(base + w.xn);
+  b->panel = reinterpret_cast<__half*>(base + w.panel);
+  b->att = reinterpret_cast<__half*>(base + w.att);
+  b->hid = reinterpret_cast<__half*>(base + w.hid);
+  b->md = reinterpret_cast<float*>(base + w.md);
+  return QI21_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cache,
+                 const float* x_prefix, const float* mods0, float* x_layers, void* workspace,
+                 size_t ws_bytes, void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (cache == nullptr || x_prefix == nullptr || mods0 == nullptr) return fail(QI21_ERR_ARG, "null pointer");
+  if (!same_geom(*g, cache->g)) return fail(QI21_ERR_SHAPE, "the cache was made for another geometry");
+  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
+  const int M = cache->lp;
+  PassBufs b;
+  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t H = g->dim;
+  QI21_CK(cudaMemcpyAsync(b.x, x_prefix, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
+          "x copy");
+  {
+    ProfScope ps(QI21_CLASS_MISC, s);
+    QI21_CK(launch_mods_prep(g->dim, mods0, b.md, s), "mods prep");
+  }
+  rc = run_pass(g, layers, M, true, cache, nullptr, 1, 0, b, x_layers, s);
+  if (rc == QI21_OK) cache->filled = true;
+  return rc;
+}
+
+int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
+                    int32_t nseq, const float* x_in, float* x_out, const float* mods, float* x_layers,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (caches == nullptr || x_in == nullptr || x_out == nullptr || mods == nullptr)
+    return fail(QI21_ERR_ARG, "null pointer");
+  if (nseq < 1 || nseq > kMaxSeq) return fail(QI21_ERR_ARG, "nseq %d outside [1, %d]", nseq, kMaxSeq);
+  int n = -1;
+  for (int q = 0; q < nseq; ++q) {
+    const qi21_kvcache* c = caches[q];
+    if (c == nullptr) return fail(QI21_ERR_ARG, "null cache %d", q);
+    if (!same_geom(*g, c->g)) return fail(QI21_ERR_SHAPE, "cache %d was made for another geometry", q);
+    if (!c->filled) return fail(QI21_ERR_STATE, "cache %d has not been prefilled", q);
+    if (n < 0) n = c->n;
+    if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
+  }
+  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
+  const int M = nseq * n;
+  PassBufs b;
+  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t H = g->dim;
+  if (x_out != x_in)
+    QI21_CK(cudaMemcpyAsync(x_out, x_in, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
+            "x copy");
+  b.x = x_out;
+  {
+    ProfScope ps(QI21_CLASS_MISC, s);
+    QI21_CK(launch_mods_prep(g->dim, mods, b.md, s), "mods prep");
+  }
+  return run_pass(g, layers, M, false, nullptr, caches, nseq, n, b, x_layers, s);
+}
+
+int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache,
+              const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
+              size_t ws_bytes, void* stream) {
+  const qi21_kvcache* cs[1] = {cache};
+  if (cache == nullptr) return fail(QI21_ERR_ARG, "null cache");
+  return qi21_step_batch(g, layers, cs, 1, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream);
+}
+
+// ------------------------------------------------------ single operations --
+
+int qi21_op_rowop(int32_t rows, int32_t dim, float eps, float* x, const float* y, const float* gate_t,
+                  const float* scale, void* xn, void* stream) {
+  if (rows < 0 || dim <= 0 || dim % 4 || dim > 8192) return fail(QI21_ERR_SHAPE, "rows %d dim %d", rows, dim);
+  if (rows == 0) return QI21_OK;  // empty input: nothing to do
+  if (x == nullptr || (y && !gate_t) || (xn && !scale) || (!y && !xn)) return fail(QI21_ERR_ARG, "null pointer");
+  QI21_CK(launch_rowop(rows, dim, eps, x, y, gate_t, scale, static_cast<__half*>(xn),
+                       static_cast<cudaStream_t>(stream)),
+          "rowop");
+  return QI21_OK;
+}
+
+int qi21_op_mods_prep(int32_t dim, const float* mods, float* md, void* stream) {
+  if (dim <= 0) return fail(QI21_ERR_SHAPE, "dim %d", dim);
+  if (!mods || !md) return fail(QI21_ERR_ARG, "null pointer");
+  QI21_CK(launch_mods_prep(dim, mods, md, static_cast<cudaStream_t>(stream)), "mods prep");
+  return QI21_OK;
+}
+
+int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* out,
+                 int32_t ldo, const float* gate_t, void* stream) {
+  if (epi < 0 || epi > 3) return fail(QI21_ERR_ARG, "epilogue %d", epi);
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 64) return fail(QI21_ERR_SHAPE, "M %d N %d K %d", M, N, K);
+  if (M == 0) return QI21_OK;
+  if (!A || !B || !out || (epi == EPI_RESID && !gate_t)) return fail(QI21_ERR_ARG, "null pointer");
+  const int cols = epi == EPI_SWIGLU ? N / 2 : N;
+  if (ldo < cols || ldo % 8) return fail(QI21_ERR_SHAPE, "ldo %d", ldo);
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(QI21_ERR_ARG, "A, B and out must be 16-byte aligned");
+  if (M == 0) return QI21_OK;
+  GemmPlan p;
+  QI21_CK(make_gemm_plan(&p, epi, M, N, K, static_cast<const __half*>(A), static_cast<const __half*>(B), out,
+                         ldo, gate_t),
+          "gemm plan");
+  QI21_CK(launch_gemm(p, static_cast<cudaStream_t>(stream)), "gemm");
+  return QI21_OK;
+}
+
+int qi21_op_qkrope(int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
+                   const float* norm_k, const float* cos_, const float* sin_, void* stream) {
+  if (rows < 0 || heads <= 0) return fail(QI21_ERR_SHAPE, "rows %d heads %d", rows, heads);
+  if (rows == 0) return QI21_OK;
+  if (!panel || !norm_q || !norm_k || !cos_ || !sin_) return fail(QI21_ERR_ARG, "null pointer");
+  RopeTables t{};
+  t.nsrc = 1;
+  t.src[0] = RopeSrc{cos_, sin_, 0};
+  QI21_CK(launch_qkrope(rows, heads, eps, static_cast<__half*>(panel), norm_q, norm_k, t,
+                        static_cast<cudaStream_t>(stream)),
+          "qkrope");
+  return QI21_OK;
+}
+
+int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void* stream) {
+  if (rows < 0 || dim <= 0 || dim % 8) return fail(QI21_ERR_SHAPE, "rows %d dim %d", rows, dim);
+  if (rows == 0) return QI21_OK;
+  if (!panel || !kv) return fail(QI21_ERR_ARG, "null pointer");
+  QI21_CK(launch_kvcopy(rows, dim, static_cast<const __half*>(panel), static_cast<__half*>(kv),
+                        static_cast<cudaStream_t>(stream)),
+          "kvcopy");
+  return QI21_OK;
+}
+
+int qi21_op_attention(int32_t nq, int32_t heads, const void* panel, const void* kv_pre, int32_t n_pre,
+                      int32_t n_own, const uint32_t* vis, void* out, void* stream) {
+  if (nq < 0 || heads <= 0 || n_pre < 0 || n_own < 0) return fail(QI21_ERR_SHAPE, "bad sizes");
+  if (nq > n_own) return fail(QI21_ERR_SHAPE, "nq %d > own rows %d (queries are panel rows)", nq, n_own);
+  if (nq == 0) return QI21_OK;
+  if (!panel || !out || (n_pre > 0 && !kv_pre)) return fail(QI21_ERR_ARG, "null pointer");
+  AttnArgs a{};
+  a.panel = static_cast<const __half*>(panel);
+  a.out = static_cast<__half*>(out);
+  a.heads = heads;
+  a.nseq = 1;
+  a.seq[0] = AttnSeq{static_cast<const __half*>(kv_pre), n_pre, 0, nq, 0, n_own, vis};
+  QI21_CK(launch_attention(a, static_cast<cudaStream_t>(stream)), "attention");
+  return QI21_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Launchers shared between the kernel translation units and the C ABI
+// (api.cu). Host-only declarations; no torch types anywhere.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qi21 {
+
+// ------------------------------------------------------------ row kernels --
+
+// md = [s1 | tanh g1 | s2 | tanh g2]
+cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t s);
+
+// if y: x += gate_t * y; if xn: xn = f16(LN(x)(1 + scale))
+cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y,
+                         const float* gate_t, const float* scale, __half* xn, cudaStream_t s);
+
+// Per-row RoPE table source: rows [row0, row0 + rows) use cos/sin + (r - row0)*64.
+struct RopeSrc {
+  const float* cos_;
+  const float* sin_;
+  int row0;
+};
+constexpr int kMaxSeq = 8;
+struct RopeTables {
+  int nsrc;
+  RopeSrc src[kMaxSeq];
+};
+
+// In place on panel f16 [rows][3H]: q, k RMSNorm * w then interleaved RoPE.
+cudaError_t launch_qkrope(int rows, int heads, float eps, __half* panel, const float* norm_q,
+                          const float* norm_k, const RopeTables& tabs, cudaStream_t s);
+
+// kv f16 [rows][2H] = panel[:, H:3H]
+cudaError_t launch_kvcopy(int rows, int dim, const __half* panel, __half* kv, cudaStream_t s);
+
+// w13 interleave: dst [2I][H] from gate [I][H], up [I][H], 64-row blocks.
+cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half* up, __half* dst,
+                            cudaStream_t s);
+
+// ------------------------------------------------------------------ GEMM ----
+
+enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3 };
+
+struct GemmPlan {
+  CUtensorMap tmA;  // A f16 [M][K], box 64 x 128, 128B swizzle
+  CUtensorMap tmB;  // B f16 [N][K], box 64 x BN, 128B swizzle
+  int M, N, K, bn, epi, ldo;
+  void* out;
+  const float* gate;
+};
+
+// Encode the tensor maps of C = A B^T. Returns cudaSuccess or an error.
+cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
+                           const __half* B, void* out, int ldo, const float* gate);
+cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s);
+
+// -------------------------------------------------------------- attention --
+
+struct AttnSeq {
+  const __half* kv_pre;  // [n_pre][2H] K then V, or null
+  int n_pre;
+  int q_row0;    // first query row in the panel / output
+  int nq;        // query rows
+  int own_row0;  // first own-key row in the panel
+  int n_own;     // own keys
+  const uint32_t* vis;  // [nq] leading-run visibility, or null (all keys)
+};
+
+struct AttnArgs {
+  const __half* panel;  // [.][3H]: q at 0, k at H, v at 2H
+  __half* out;          // [.][H]
+  int heads;
+  int nseq;
+  AttnSeq seq[kMaxSeq];
+};
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------------- device ----
+
+int sm_count();
+// Each translation unit whose kernels wait on mbarriers keeps its own device
+// status word; these read and clear them (after a device synchronise).
+unsigned int gemm_status_read_clear();
+unsigned int read_and_clear_status();
+
+}  // namespace qi21

@@ -1,0 +1,348 @@
+// tcgen05 GEMM for the block's four projections: C = A B^T with A f16
+// [M][K] (activations) and B f16 [N][K] (nn.Linear weights), both K-major,
+// f32 accumulation in TMEM, fused epilogues:
+//   EPI_F16    qkv panel store                (gpu_wgpu/qi21.rs, zi_mm f16)
+//   EPI_RESID  x += tanh(g) * acc on the f32 residual stream (the O and down
+//              projections followed by Qi21Dit::gated_add)
+//   EPI_SWIGLU silu(gate) * up on the interleaved gate/up plane
+//              (qwen_image21.rs, block_cpu: silu(gate) * proj)
+//   EPI_F32    plain f32 store (single-operation checks)
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0     TMA producer: A 128x64 and B BNx64 tiles (128-byte swizzle)
+//              into a STAGES-deep shared-memory ring (full/empty mbarriers)
+//   warp 1     TMEM allocator and single-thread MMA issuer
+//              (tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16)
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quadrant, fused op,
+//              128-bit stores; two TMEM accumulators so the epilogue of tile
+//              i overlaps the MMAs of tile i+1.
+#include <algorithm>
+#include <cstdio>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qi21 {
+
+// Status word of this translation unit's kernels (a wait that gave up).
+static __device__ unsigned int s_gemm_status = 0;
+
+unsigned int gemm_status_read_clear() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, s_gemm_status, sizeof v);
+  cudaMemcpyToSymbol(s_gemm_status, &z, sizeof z);
+  return v;
+}
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
+};
+
+struct EpiArgs {
+  void* out;
+  int ldo;
+  const float* gate;
+};
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
+
+template <int BN, int EPI>
+__device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0,
+                                              const EpiArgs& ep) {
+  const bool live = row < M;
+  if constexpr (EPI == EPI_SWIGLU) {
+    __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
+#pragma unroll 1
+    for (int p = 0; p < BN / 128; ++p) {
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t g[32], u[32];
+        tmem_ld32(tbase + p * 128 + c * 32, g);
+        tmem_ld32(tbase + p * 128 + 64 + c * 32, u);
+        tmem_ld_wait(g);
+        tmem_ld_wait(u);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(out + p * 64 + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 8 * j + 2 * e;
+              const float h0 = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+              const float h1 = silu_f(__uint_as_float(g[i + 1])) * __uint_as_float(u[i + 1]);
+              w[e] = pack_half2(h0, h1);
+            }
+            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait(r);
+      if (!live) continue;
+      const int col = n0 + c * 32;
+      if constexpr (EPI == EPI_F16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(ep.out) +
+                                              static_cast<size_t>(row) * ep.ldo + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dst[j] = make_uint4(pack_half2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                              pack_half2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                              pack_half2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                              pack_half2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+        }
+      } else if constexpr (EPI == EPI_F32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) +
+                                                static_cast<size_t>(row) * ep.ldo + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      } else {  // EPI_RESID
+        float4* xp = reinterpret_cast<float4*>(static_cast<float*>(ep.out) +
+                                               static_cast<size_t>(row) * ep.ldo + col);
+        const float4* gp = reinterpret_cast<const float4*>(ep.gate + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 x = xp[j];
+          const float4 gv = __ldg(gp + j);
+          x.x = fmaf(gv.x, __uint_as_float(r[4 * j + 0]), x.x);
+          x.y = fmaf(gv.y, __uint_as_float(r[4 * j + 1]), x.y);
+          x.z = fmaf(gv.z, __uint_as_float(r[4 * j + 2]), x.z);
+          x.w = fmaf(gv.w, __uint_as_float(r[4 * j + 3]), x.w);
+          xp[j] = x;
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   int M, int N, int K, EpiArgs ep) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (M + kBM - 1) / kBM;
+  const int num_tiles = num_m * (N / BN);
+  const int nk = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const int m0 = (t % num_m) * kBM;
+        const int n0 = (t / num_m) * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, &s_gemm_status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * kBK, m0);
+          tma_load_2d(sa + C::kABytes, &tmB, &full[s], kb * kBK, n0);
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(kBM, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, &s_gemm_status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, &s_gemm_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::kStageBytes);
+          const uint64_t adesc = sdesc_sw128(sa);
+          const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma_f16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const int m0 = (t % num_m) * kBM;
+      const int n0 = (t / num_m) * BN;
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      gemm_epilogue<BN, EPI>(tbase, m0 + q * 32 + lane, M, n0, ep);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host ----
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D f16 tensor [outer][inner] with the given row pitch; box inner x outer.
+static cudaError_t encode_f16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
+                           const __half* B, void* out, int ldo, const float* gate) {
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->epi = epi;
+  p->ldo = ldo;
+  p->out = out;
+  p->gate = gate;
+  p->bn = (N % 256 == 0) ? 256 : 128;
+  cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
+  if (e != cudaSuccess) return e;
+  return encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn);
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
+  using C = GemmCfg<BN>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / BN);
+  const int grid = std::min(tiles, sm_count());
+  EpiArgs ep{p.out, p.ldo, p.gate};
+  gemm_tc_kernel<BN, EPI><<<grid, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.M, p.N, p.K, ep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
+  if (p.M <= 0) return cudaSuccess;
+  if (p.bn == 256) {
+    switch (p.epi) {
+      case EPI_F16: return launch_t<256, EPI_F16>(p, s);
+      case EPI_F32: return launch_t<256, EPI_F32>(p, s);
+      case EPI_RESID: return launch_t<256, EPI_RESID>(p, s);
+      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU>(p, s);
+    }
+  } else {
+    switch (p.epi) {
+      case EPI_F16: return launch_t<128, EPI_F16>(p, s);
+      case EPI_F32: return launch_t<128, EPI_F32>(p, s);
+      case EPI_RESID: return launch_t<128, EPI_RESID>(p, s);
+      case EPI_SWIGLU: return launch_t<128, EPI_SWIGLU>(p, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace qi21

@@ -1,0 +1,206 @@
+// Row kernels of the block: the modulation prep, the fused gated residual +
+// modulated LayerNorm, the per-head qk RMSNorm + interleaved RoPE, the K/V
+// cache copy and the gate/up plane interleave. All HBM-bound: 128-bit
+// coalesced loads/stores, one CTA per row where a row reduction is needed.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qi21 {
+
+// ------------------------------------------------------------ mods prep ----
+// [s1 | g1 | s2 | g2] -> [s1 | tanh g1 | s2 | tanh g2] (gpu_wgpu/qi21.rs,
+// mods_dev: the gate chunks tanh-ed once per pass).
+__global__ void mods_prep_kernel(int dim, const float* __restrict__ mods, float* __restrict__ md) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 4 * dim) return;
+  const int chunk = i / dim;
+  const float v = mods[i];
+  md[i] = (chunk == 1 || chunk == 3) ? tanhf(v) : v;
+}
+
+cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t s) {
+  const int n = 4 * dim;
+  mods_prep_kernel<<<(n + 255) / 256, 256, 0, s>>>(dim, mods, md);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- rowop ----
+// One 128-thread CTA per row, the row held in registers (dim <= 8192):
+//   if y:  x += gate_t * y            (qwen_image21.rs, Qi21Dit::gated_add)
+//   if xn: xn = f16(LN(x) (1 + scale)) (Qi21Dit::norm_mod; affine-free LN,
+//          biased variance, two passes over the registers in f32)
+constexpr int kRowThreads = 128;
+constexpr int kRowMaxVec = 16;  // float4 per thread -> dim <= 8192
+
+__device__ __forceinline__ float block_sum_128(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  return red[0] + red[1] + red[2] + red[3];
+}
+
+__global__ void __launch_bounds__(kRowThreads) rowop_kernel(int dim, float eps, float* __restrict__ x,
+                                                            const float* __restrict__ y,
+                                                            const float* __restrict__ gate_t,
+                                                            const float* __restrict__ scale,
+                                                            __half* __restrict__ xn) {
+  __shared__ float red[4];
+  const size_t row = blockIdx.x;
+  const int nv = dim >> 2;
+  float4* x4 = reinterpret_cast<float4*>(x + row * dim);
+  float4 v[kRowMaxVec];
+#pragma unroll
+  for (int j = 0; j < kRowMaxVec; ++j) {
+    const int idx = threadIdx.x + j * kRowThreads;
+    if (idx < nv) {
+      float4 a = x4[idx];
+      if (y != nullptr) {
+        const float4 b = reinterpret_cast<const float4*>(y + row * dim)[idx];
+        const float4 g = reinterpret_cast<const float4*>(gate_t)[idx];
+        a.x = fmaf(g.x, b.x, a.x);
+        a.y = fmaf(g.y, b.y, a.y);
+        a.z = fmaf(g.z, b.z, a.z);
+        a.w = fmaf(g.w, b.w, a.w);
+        x4[idx] = a;
+      }
+      v[j] = a;
+    }
+  }
+  if (xn == nullptr) return;
+  float sm = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxVec; ++j)
+    if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+  const float mean = block_sum_128(sm, red) / static_cast<float>(dim);
+  float sq = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRowMaxVec; ++j) {
+    if (threadIdx.x + j * kRowThreads < nv) {
+      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
+      sq += (a * a + b * b) + (c * c + d * d);
+    }
+  }
+  const float inv = rsqrtf(block_sum_128(sq, red) / static_cast<float>(dim) + eps);
+  uint2* o2 = reinterpret_cast<uint2*>(xn + row * dim);
+#pragma unroll
+  for (int j = 0; j < kRowMaxVec; ++j) {
+    const int idx = threadIdx.x + j * kRowThreads;
+    if (idx < nv) {
+      const float4 sc = reinterpret_cast<const float4*>(scale)[idx];
+      uint2 out;
+      out.x = pack_half2((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
+      out.y = pack_half2((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
+      o2[idx] = out;
+    }
+  }
+}
+
+cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
+                         const float* scale, __half* xn, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  rowop_kernel<<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- qkrope ----
+// One 256-thread CTA per panel row; each warp takes head vectors of q then
+// k (128 f16 = 4 per lane), RMSNorm over the 128 values (warp shuffle), the
+// weight, then rotates the pairs (2j, 2j+1) by the row's angle j
+// (qwen_image21.rs, Qi21Dit::qk_norm_rope; gpu_wgpu/qi21.rs, zi_qkrope).
+__global__ void __launch_bounds__(256) qkrope_kernel(int heads, float eps, __half* __restrict__ panel,
+                                                     const float* __restrict__ norm_q,
+                                                     const float* __restrict__ norm_k,
+                                                     RopeTables tabs) {
+  const int row = blockIdx.x;
+  int si = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxSeq; ++i)
+    if (i < tabs.nsrc && row >= tabs.src[i].row0) si = i;
+  const size_t trow = static_cast<size_t>(row - tabs.src[si].row0) * 64;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const float2 c = reinterpret_cast<const float2*>(tabs.src[si].cos_ + trow)[lane];
+  const float2 sn = reinterpret_cast<const float2*>(tabs.src[si].sin_ + trow)[lane];
+  const float4 wq = reinterpret_cast<const float4*>(norm_q)[lane];
+  const float4 wk = reinterpret_cast<const float4*>(norm_k)[lane];
+  const int H = heads * 128;
+  __half* base = panel + static_cast<size_t>(row) * 3 * H;
+  for (int v = warp; v < 2 * heads; v += 8) {
+    uint2* p = reinterpret_cast<uint2*>(base + v * 128 + lane * 4);
+    const uint2 raw = *p;
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    float ss = (lo.x * lo.x + lo.y * lo.y) + (hi.x * hi.x + hi.y * hi.y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss * (1.f / 128.f) + eps);
+    const float4 w = v < heads ? wq : wk;
+    const float a0 = lo.x * inv * w.x, a1 = lo.y * inv * w.y;
+    const float a2 = hi.x * inv * w.z, a3 = hi.y * inv * w.w;
+    uint2 out;
+    out.x = pack_half2(a0 * c.x - a1 * sn.x, a0 * sn.x + a1 * c.x);
+    out.y = pack_half2(a2 * c.y - a3 * sn.y, a2 * sn.y + a3 * c.y);
+    *p = out;
+  }
+}
+
+cudaError_t launch_qkrope(int rows, int heads, float eps, __half* panel, const float* norm_q,
+                          const float* norm_k, const RopeTables& tabs, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  qkrope_kernel<<<rows, 256, 0, s>>>(heads, eps, panel, norm_q, norm_k, tabs);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- kvcopy ----
+// The K|V columns of the panel -> the layer's cache row, 16 B per thread
+// (gpu_wgpu/qi21.rs, qi_kvcopy).
+__global__ void kvcopy_kernel(int rows, int dim, const __half* __restrict__ panel,
+                              __half* __restrict__ kv) {
+  const int per_row = (2 * dim) / 8;  // uint4 per cache row
+  const size_t total = static_cast<size_t>(rows) * per_row;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i / per_row;
+    const int c = static_cast<int>(i - r * per_row);
+    const uint4 v = reinterpret_cast<const uint4*>(panel + r * 3 * dim + dim)[c];
+    reinterpret_cast<uint4*>(kv + r * 2 * dim)[c] = v;
+  }
+}
+
+cudaError_t launch_kvcopy(int rows, int dim, const __half* panel, __half* kv, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const size_t total = static_cast<size_t>(rows) * (2 * dim / 8);
+  const int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, 152 * 16));
+  kvcopy_kernel<<<grid, 256, 0, s>>>(rows, dim, panel, kv);
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------- pack w13 ----
+// Interleave gate and up in 64-row blocks so that every 128-row slice of the
+// plane holds a matching (gate, up) pair for the SwiGLU epilogue.
+__global__ void pack_w13_kernel(int inter, int dim, const __half* __restrict__ gate,
+                                const __half* __restrict__ up, __half* __restrict__ dst) {
+  const int r = blockIdx.x;  // destination row in [0, 2I)
+  const int j = r >> 7;
+  const int w = r & 127;
+  const __half* src = (w < 64) ? gate + static_cast<size_t>(64 * j + w) * dim
+                               : up + static_cast<size_t>(64 * j + (w - 64)) * dim;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * dim);
+  for (int c = threadIdx.x; c < dim / 8; c += blockDim.x) d4[c] = s4[c];
+}
+
+cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half* up, __half* dst,
+                            cudaStream_t s) {
+  pack_w13_kernel<<<2 * inter, 256, 0, s>>>(inter, dim, gate, up, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace qi21

@@ -1,0 +1,295 @@
+/*
+ * qi21.h -- C ABI of the GB300 (sm_103a) Qwen-Image-2.1 single-stream DiT
+ * block: prefill of the prompt prefix into a per-layer K/V cache, and the
+ * denoiser step of the target rows against [cached prefix, own rows].
+ *
+ * Semantics follow the CPU-exact path of the docs.rs page
+ * "cortiq_engine/qwen_image21.rs" (v0.8.4): Seg / Qi21Layout (positions,
+ * block_ids), rope_tables, Qi21Dit::block_cpu, Qi21Dit::prefill and
+ * Qi21Dit::step_cpu. The device contract (prefill keeps each layer's
+ * post-RoPE K/V; step reads it) follows the module notes of
+ * "gpu_wgpu/qi21.rs" (v0.8.3).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device pointers on the current
+ *    device; "host" pointers are ordinary host memory. The caller owns every
+ *    buffer it passes (weights, activations, workspace) and the stream. The
+ *    library owns only qi21_kvcache objects.
+ *  - Matrices are row-major. Weights are in nn.Linear layout [out][in].
+ *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and is asynchronous: a return of QI21_OK means
+ *    "validated and enqueued".
+ *  - On any error the host can detect (bad argument, shape, geometry,
+ *    mask, too-small workspace) nothing is written and nothing is enqueued;
+ *    the function returns a negative QI21_ERR_* and qi21_last_error()
+ *    (thread-local) describes it. This mirrors the page's "decline, no
+ *    partial results" convention.
+ *  - Every spin-wait inside the kernels gives up after about 2 s and raises
+ *    a device status word; qi21_device_status() reads and clears it.
+ */
+#ifndef QI21_H
+#define QI21_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QI21_OK 0
+#define QI21_ERR_ARG (-1)       /* null pointer, negative size, bad enum */
+#define QI21_ERR_SHAPE (-2)     /* lengths/row counts that do not agree */
+#define QI21_ERR_GEOM (-3)      /* geometry outside what the kernels take */
+#define QI21_ERR_MASK (-4)      /* visibility not a non-decreasing leading run */
+#define QI21_ERR_OOM (-5)       /* device allocation failed */
+#define QI21_ERR_CUDA (-6)      /* a CUDA runtime call failed */
+#define QI21_ERR_STATE (-7)     /* cache not prefilled / layer out of range */
+#define QI21_ERR_WORKSPACE (-8) /* workspace too small or misaligned */
+#define QI21_ERR_DEVICE (-9)    /* a kernel raised its status word (timeout) */
+
+/* Segment kinds of a layout (qwen_image21.rs, enum Seg). */
+#define QI21_SEG_TEXT 0  /* a = number of text rows, b unused */
+#define QI21_SEG_IMAGE 1 /* a = h, b = w; h*w rows in raster order */
+
+/* Model geometry (qwen_image21.rs, Qi21Config). Kernel limits (the page's
+ * geom_ok, gpu_wgpu/qi21.rs): head_dim == 128, heads*head_dim == dim,
+ * dim % 128 == 0, 128 <= dim <= 8192, mlp_hidden % 64 == 0, axes even and
+ * summing to head_dim, layers >= 1. Compute type: f16 operands, f32
+ * accumulation, f32 residual stream. */
+typedef struct qi21_geom {
+  int32_t dim;        /* H */
+  int32_t heads;      /* nh */
+  int32_t head_dim;   /* hd, must be 128 */
+  int32_t mlp_hidden; /* I */
+  int32_t layers;     /* L */
+  int32_t axes[3];    /* RoPE axis widths (frame, h, w), e.g. 16, 56, 56 */
+  float eps;          /* LayerNorm / RMSNorm epsilon, e.g. 1e-6 */
+  float theta;        /* RoPE base, e.g. 10000 */
+} qi21_geom;
+
+/* One run of the joint sequence (qwen_image21.rs, enum Seg). The last
+ * segment of a layout is the target image block; the rest is the prefix. */
+typedef struct qi21_seg {
+  int32_t kind;
+  int32_t a;
+  int32_t b;
+} qi21_seg;
+
+/* Device planes of one block, as produced by qi21_pack_layer.
+ *   wqkv  f16 [3H][H]  rows q (H), k (H), v (H)
+ *   wo    f16 [H][H]
+ *   w13   f16 [2I][H]  gate/up interleaved in 64-row blocks:
+ *                      rows [128j, 128j+64) = gate rows [64j, 64j+64),
+ *                      rows [128j+64, 128j+128) = up rows [64j, 64j+64)
+ *   w2    f16 [H][I]   (down)
+ *   norm_q, norm_k  f32 [128] per-head RMSNorm weights (used as is)
+ * Tensor names on the page: attn.to_q/to_k/to_v, attn.to_out.0,
+ * img_mlp.gate_layer (gate), img_mlp.proj (up), img_mlp.out (down),
+ * attn.norm_q, attn.norm_k (qwen_image21.rs, Qi21Dit::from_cmf). */
+typedef struct qi21_layer {
+  const void* wqkv;
+  const void* wo;
+  const void* w13;
+  const void* w2;
+  const float* norm_q;
+  const float* norm_k;
+} qi21_layer;
+
+/* Opaque per-prompt cache: L layers of post-RoPE K|V, f16 [lp][2H] each
+ * (K in columns [0, H), V in [H, 2H)), plus the layout, the prefix
+ * visibility and the RoPE tables of the prefix rows and of the target rows
+ * at the positions after THIS prefix (qwen_image21.rs, struct Qi21Prefix). */
+typedef struct qi21_kvcache qi21_kvcache;
+
+/* ------------------------------------------------------------- host ---- */
+
+/* Text of the last error on this thread ("" if none). Never NULL. */
+const char* qi21_last_error(void);
+
+/* Library version string. */
+const char* qi21_version(void);
+
+/* 0 if the geometry is one the kernels take, else QI21_ERR_GEOM / _ARG. */
+int qi21_geom_check(const qi21_geom* g);
+
+/* Row counts of a layout (qwen_image21.rs, Qi21Layout::total, prefix_len,
+ * target, validate): the last segment must be a non-empty image block and
+ * the prefix non-empty. Any output pointer may be NULL. Host only. */
+int qi21_layout_rows(const qi21_seg* segs, int32_t nseg, int32_t* total, int32_t* prefix,
+                     int32_t* target);
+
+/* Index construction of a layout, on the host (qwen_image21.rs,
+ * Qi21Layout::positions, Qi21Layout::block_ids, rope_tables, and the
+ * visibility end[i] of Qi21Dit::prefill). Outputs (each may be NULL):
+ *   pos       int64 [total][3]   (frame, h, w)
+ *   block_ids int32 [total]      -1 for text, else the image-block id
+ *   vis       uint32 [prefix]    prefix row i sees keys [0, vis[i])
+ *   cos, sin  f32 [total][hd/2]  hd = axes[0]+axes[1]+axes[2]; f32
+ *             frequencies 1/theta^(2i/d), f32 angle, f32 cos/sin
+ * Integers are exact; the tables are within a few ulp of any other f32
+ * evaluation of the same formula. */
+int qi21_layout_indices(const qi21_seg* segs, int32_t nseg, const int32_t axes[3], float theta,
+                        int64_t* pos, int32_t* block_ids, uint32_t* vis, float* cos_,
+                        float* sin_);
+
+/* Bytes of one layer's packed planes (wqkv + wo + w13 + w2, f16, each
+ * 256-byte aligned). */
+size_t qi21_layer_plane_bytes(const qi21_geom* g);
+
+/* Workspace bytes of a pass over up to `max_rows` rows (prefill rows, or
+ * the sum of the target rows of a step batch). */
+size_t qi21_workspace_bytes(const qi21_geom* g, int32_t max_rows);
+
+/* ----------------------------------------------------------- device ---- */
+
+/* Pack one layer's weights (device f16, nn.Linear layout: wq/wk/wv/wo
+ * [H][H], wgate/wup [I][H], wdown [H][I]; norm_q/norm_k device f32 [128])
+ * into `planes` (device, >= qi21_layer_plane_bytes, 256-byte aligned) and
+ * fill `out` with pointers into it (norm_q/norm_k are referenced, not
+ * copied). Enqueued on `stream`. */
+int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const void* wv,
+                    const void* wo, const void* wgate, const void* wup, const void* wdown,
+                    const float* norm_q, const float* norm_k, void* planes, size_t plane_bytes,
+                    qi21_layer* out, void* stream);
+
+/* Allocate a cache for the layout (library-owned device memory; the
+ * layout's tables are built on the host and copied synchronously). The
+ * analogue of the page's per-prompt program (gpu_wgpu/qi21.rs, struct
+ * Prog). Returns QI21_ERR_OOM if the device is out of memory. */
+int qi21_kvcache_alloc(const qi21_geom* g, const qi21_seg* segs, int32_t nseg,
+                       qi21_kvcache** out);
+
+/* Free a cache (NULL is a no-op); synchronises the device first. The
+ * analogue of release_key (gpu_wgpu/qi21.rs). */
+void qi21_kvcache_free(qi21_kvcache* c);
+
+/* Prefix rows, target rows and layers of a cache; any pointer may be NULL. */
+int qi21_kvcache_info(const qi21_kvcache* c, int32_t* lp, int32_t* n, int32_t* layers);
+
+/* Device pointer of layer `layer`'s K|V block, f16 [lp][2H] (read-only use
+ * by the caller: parity checks, saving a prompt). */
+int qi21_kvcache_layer(const qi21_kvcache* c, int32_t layer, const void** kv);
+
+/* Prefill (qwen_image21.rs, Qi21Dit::prefill; gpu_wgpu/qi21.rs, prefill and
+ * blocks()): the prefix rows x_prefix (device f32 [lp][H], read only)
+ * through every block with the t = 0 modulation `mods0` (device f32 [4H],
+ * raw [scale1|gate1|scale2|gate2]; the gates are tanh-ed on the device) and
+ * the block-causal mask; each layer's post-RoPE K|V is written to the
+ * cache. The last layer stops after its cache write (its output feeds
+ * nothing). x_layers (device f32 [L][lp][H], or NULL) receives the hidden
+ * state after each block 0 .. L-2. `layers` is a host array of L planes.
+ * `workspace` (device, 256-byte aligned) must hold
+ * qi21_workspace_bytes(g, lp). */
+int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cache,
+                 const float* x_prefix, const float* mods0, float* x_layers, void* workspace,
+                 size_t ws_bytes, void* stream);
+
+/* Step (qwen_image21.rs, Qi21Dit::step_cpu, the block loop;
+ * gpu_wgpu/qi21.rs, step): the target rows x_in (device f32 [n][H]) through
+ * every block against [cached prefix, own rows], every key visible, with
+ * the step modulation `mods` (device f32 [4H], raw). The result is written
+ * to x_out (device f32 [n][H]; may equal x_in). x_layers (device f32
+ * [L][n][H] or NULL) receives the hidden state after every block.
+ * workspace >= qi21_workspace_bytes(g, n). */
+int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache,
+              const float* x_in, float* x_out, const float* mods, float* x_layers,
+              void* workspace, size_t ws_bytes, void* stream);
+
+/* Step of `nseq` (1..8) sequences that share the weights, the modulation
+ * and the target row count n (a classifier-free-guidance pair: one latent,
+ * two prompts). Sequence s has its own cache caches[s] (own prefix, own
+ * target RoPE) and rows [s*n, (s+1)*n) of x_in/x_out (device f32
+ * [nseq*n][H]); the GEMMs run on the stacked nseq*n rows and the attention
+ * per sequence. x_layers is [L][nseq*n][H] or NULL.
+ * workspace >= qi21_workspace_bytes(g, nseq*n). */
+int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers,
+                    const qi21_kvcache* const* caches, int32_t nseq, const float* x_in,
+                    float* x_out, const float* mods, float* x_layers, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* Reads and clears the device status word (0 = fine; nonzero = a kernel
+ * gave up waiting). Synchronises the device. */
+int qi21_device_status(void);
+
+/* Kernel classes of a pass, for qi21_profile_read. */
+#define QI21_CLASS_ROWOP 0     /* modulated LayerNorm rows */
+#define QI21_CLASS_QKV 1       /* qkv projection (tcgen05 GEMM, f16 panel) */
+#define QI21_CLASS_QKROPE 2    /* qk RMSNorm + RoPE */
+#define QI21_CLASS_KVCOPY 3    /* K|V cache write (prefill) */
+#define QI21_CLASS_ATTENTION 4 /* flash attention */
+#define QI21_CLASS_O 5         /* output projection + gated residual */
+#define QI21_CLASS_GATEUP 6    /* gate/up projection + SwiGLU */
+#define QI21_CLASS_DOWN 7      /* down projection + gated residual */
+#define QI21_CLASS_MISC 8      /* modulation prep */
+#define QI21_NCLASS 9
+
+/* Per-class device timing of the passes, the analogue of the page's
+ * per-class step times (gpu_wgpu/qi21.rs, class_times). on != 0 starts
+ * recording two CUDA events (on the launch stream) around every kernel a
+ * pass launches and forgets earlier records; on == 0 stops. Host-side
+ * overhead only; the kernels are unchanged. */
+int qi21_profile_enable(int on);
+
+/* Per class: ms = summed device time of the launches recorded since the
+ * last enable/read (synchronises on them; NULL to skip), launches = kernels
+ * launched by passes since the library was loaded (counted always).
+ * Arrays of QI21_NCLASS. Clears the records. */
+int qi21_profile_read(float* ms, int64_t* launches);
+
+/* ------------------------------------------------- single operations ---- */
+/* Kernel-level entry points (the same kernels the passes launch), for
+ * per-operation parity checks and profiling. All pointers are device. */
+
+/* xn = f16(LN(x)(1 + scale)) per row; if y != NULL it first does
+ * x += gate_t * y in place (gate_t = tanh of the raw gate, f32 [H]).
+ * x f32 [rows][H], y f32 [rows][H], scale f32 [H], xn f16 [rows][H] (may be
+ * NULL when y != NULL). qwen_image21.rs: Qi21Dit::norm_mod, gated_add;
+ * gpu_wgpu/qi21.rs: qi_rowop. */
+int qi21_op_rowop(int32_t rows, int32_t dim, float eps, float* x, const float* y,
+                  const float* gate_t, const float* scale, void* xn, void* stream);
+
+/* md = [s1 | tanh g1 | s2 | tanh g2] from raw mods, f32 [4H] each
+ * (gpu_wgpu/qi21.rs, mods_dev). */
+int qi21_op_mods_prep(int32_t dim, const float* mods, float* md, void* stream);
+
+/* GEMM epilogues of qi21_op_gemm. */
+#define QI21_EPI_F16 0    /* out f16 [M][ldo] = acc */
+#define QI21_EPI_F32 1    /* out f32 [M][ldo] = acc */
+#define QI21_EPI_RESID 2  /* out f32 [M][ldo] += gate_t[col] * acc */
+#define QI21_EPI_SWIGLU 3 /* out f16 [M][ldo]: col 64j+c = silu(acc[128j+c]) *
+                             acc[128j+64+c] (N = 2*I on the interleaved plane) */
+
+/* acc = A B^T with A f16 [M][K] (row stride K), B f16 [N][K] (row stride
+ * K), f32 accumulation on the tensor cores; M >= 1, N % 128 == 0,
+ * K % 64 == 0. */
+int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B,
+                 void* out, int32_t ldo, const float* gate_t, void* stream);
+
+/* In place on the panel f16 [rows][3H] (q in columns [0, H), k in [H, 2H)):
+ * per (row, head) RMSNorm * norm_q (or norm_k) over 128 values, then the
+ * interleaved RoPE of pairs (2j, 2j+1) by the row's cos/sin [rows][64]
+ * (qwen_image21.rs, Qi21Dit::qk_norm_rope; gpu_wgpu/qi21.rs, zi_qkrope). */
+int qi21_op_qkrope(int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
+                   const float* norm_k, const float* cos_, const float* sin_, void* stream);
+
+/* cache f16 [rows][2H] = panel columns [H, 3H) (gpu_wgpu/qi21.rs,
+ * qi_kvcopy). */
+int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void* stream);
+
+/* Attention of nq query rows of the panel (q at columns [0, H) of panel
+ * f16 [.][3H]) over n_pre keys from kv_pre (f16 [n_pre][2H], K then V; may
+ * be NULL when n_pre == 0) followed by the panel's own keys rows
+ * [0, n_own) (K at columns [H, 2H), V at [2H, 3H)). Query i sees keys
+ * [0, vis[i]) if vis != NULL (uint32 [nq], non-decreasing, >= 1), else all
+ * n_pre + n_own keys. out f16 [nq][H] (qwen_image21.rs, Qi21Dit::attention;
+ * gpu_wgpu/qi21.rs, qi_flash). */
+int qi21_op_attention(int32_t nq, int32_t heads, const void* panel, const void* kv_pre,
+                      int32_t n_pre, int32_t n_own, const uint32_t* vis, void* out,
+                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QI21_H */

@@ -44,6 +44,7 @@ TAG_ID = {
     "wdown": 16,
     "norm_q": 17,
     "norm_k": 18,
+    "op_test": 50,  # single-operation checks: index = a case number
 }
 
 # Segment kinds, as the library's C ABI numbers them.
@@ -219,3 +220,11 @@ def layer_weights(w: Workload, layer: int) -> dict:
     d["norm_q"] = norm_weight(w, layer, "norm_q")
     d["norm_k"] = norm_weight(w, layer, "norm_k")
     return d
+
+
+def op_tensor(seed: int, case: int, slot: int, shape, std: float = 1.0, offset: float = 0.0,
+              dtype=np.float32) -> np.ndarray:
+    """A seeded tensor for a single-operation check: stream (seed, case,
+    slot) of the "op_test" tag."""
+    count = int(np.prod(shape))
+    return normal(seed * 1000003 + case, "op_test", slot, count, std, dtype=dtype, offset=offset).reshape(shape)

@@ -1,0 +1,114 @@
+"""Host-side checks of the library (no GPU): it loads, exports every symbol
+include/qi21.h declares, rejects bad arguments with the documented codes,
+and builds positions / block ids / visibility bit-exactly like the oracle
+(RoPE tables within a few ulp)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import diffusion_transformer_denoiser_qi21_gb300 as q
+from diffusion_transformer_denoiser_qi21_gb300 import _binding as B
+from oracle import qi21_oracle as O
+from synthetic import qi21_inputs as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "qi21.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qi21_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = q.load()
+    names = _header_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B.exported_symbols()) == set(names)
+
+
+def test_version_and_no_error_initially():
+    assert b"sm_103a" in q.load().qi21_version()
+
+
+LAYOUTS = [
+    [(0, 3, 0), (1, 2, 3)],
+    [(0, 2, 0), (1, 2, 4), (0, 1, 0), (1, 1, 1)],
+    [(0, 18, 0), (1, 64, 64), (1, 64, 64)],
+    [(0, 5, 0), (1, 4, 6), (0, 3, 0), (1, 3, 2), (1, 10, 13)],
+    [(0, 1, 0), (1, 1, 1)],
+    [(1, 3, 5), (0, 4, 0), (1, 7, 2)],
+] + [S.WORKLOADS[k].segs(s) for k in S.WORKLOADS for s in range(S.WORKLOADS[k].nseq)]
+
+
+@pytest.mark.parametrize("segs", LAYOUTS)
+def test_layout_indices_match_oracle(segs):
+    pos, ids, vis, cs, sn = q.layout_indices(segs)
+    np.testing.assert_array_equal(pos, O.positions(segs))
+    np.testing.assert_array_equal(ids, O.block_ids(segs))
+    np.testing.assert_array_equal(vis, O.prefix_visibility(segs))
+    oc, osn = O.rope_tables(O.positions(segs))
+    # same f32 formula, different libm: a few ulp of values in [-1, 1]
+    assert np.max(np.abs(cs - oc)) <= 4e-7 * max(1.0, float(np.abs(pos).max()))
+    assert np.max(np.abs(sn - osn)) <= 4e-7 * max(1.0, float(np.abs(pos).max()))
+    total, lp, n = q.layout_rows(segs)
+    assert (total, lp, n) == (O.total_rows(segs), O.prefix_len(segs), O.seg_len(segs[-1]))
+
+
+@pytest.mark.parametrize("segs,code", [
+    ([(0, 3, 0)], -2),             # no target image
+    ([(1, 2, 2)], -2),             # empty prefix
+    ([(0, 3, 0), (1, 0, 4)], -2),  # empty target
+    ([(0, -1, 0), (1, 2, 2)], -1),  # negative length
+    ([(7, 1, 1), (1, 2, 2)], -1),  # unknown kind
+])
+def test_layout_errors(segs, code):
+    with pytest.raises(q.Qi21Error) as e:
+        q.layout_rows(segs)
+    assert e.value.code == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=1, head_dim=64), -3),
+    (dict(dim=256, heads=3, mlp_hidden=768, layers=1), -3),
+    (dict(dim=192, heads=1, mlp_hidden=768, layers=1, head_dim=192), -3),
+    (dict(dim=256, heads=2, mlp_hidden=700, layers=1), -3),
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=0), -3),
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=1, axes=(16, 56, 58)), -3),
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=1, axes=(15, 57, 56)), -3),
+])
+def test_geometry_errors(kw, code):
+    g = q.geom(**kw)
+    assert q.load().qi21_geom_check(C.byref(g)) == code
+    assert q.workspace_bytes(g, 10) == 0
+
+
+def test_geometry_ok_and_sizes():
+    g = q.geom(4096, 32, 12288, 32)
+    assert q.load().qi21_geom_check(C.byref(g)) == 0
+    H, I = 4096, 12288
+    assert q.layer_plane_bytes(g) == 2 * (3 * H * H + H * H + 2 * I * H + H * I)
+    M = 4096
+    per_row = 4 * H + 2 * H + 6 * H + 2 * H + 2 * I
+    assert q.workspace_bytes(g, M) >= M * per_row + 16 * H
+    assert q.workspace_bytes(g, M) < M * per_row + 16 * H + 8 * 256
+
+
+def test_device_entry_points_reject_bad_args_before_touching_the_device():
+    lib = q.load()
+    g = q.geom(256, 2, 768, 1)
+    # null cache / pointers -> ARG, nothing enqueued (no CUDA context needed)
+    assert lib.qi21_prefill(C.byref(g), None, None, None, None, None, None, 0, None) == -1
+    assert lib.qi21_step(C.byref(g), None, None, None, None, None, None, None, 0, None) == -1
+    assert lib.qi21_op_gemm(0, 128, 100, 64, 8, 8, 8, 128, None, None) == -2  # N % 128
+    assert lib.qi21_op_gemm(9, 128, 128, 64, 8, 8, 8, 128, None, None) == -1  # epilogue
+    assert lib.qi21_op_rowop(4, 6, 1e-6, 8, None, None, 8, 8, None) == -2    # dim % 4
+    assert lib.qi21_op_attention(10, 2, 8, None, 0, 5, None, 8, None) == -2  # nq > own rows
+    bad = q.geom(256, 2, 768, 1, head_dim=64)
+    assert lib.qi21_prefill(C.byref(bad), None, None, None, None, None, None, 0, None) == -3
+    assert b"head_dim" in lib.qi21_last_error()
