@@ -49,7 +49,7 @@ int sm_count() {
 
 unsigned int read_and_clear_status() {
   cudaDeviceSynchronize();
-  return gemm_status_read_clear();
+  return gemm_status_read_clear() | attn_status_read_clear();
 }
 
 // ---------------------------------------------------------- profiling ----
@@ -553,6 +553,7 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
     }
     AttnArgs aa{};
     aa.panel = b.panel;
+    aa.panel_rows = M;
     aa.out = b.att;
     aa.heads = g->heads;
     if (prefill) {
@@ -767,6 +768,7 @@ int qi21_op_attention(int32_t nq, int32_t heads, const void* panel, const void* 
   if (!panel || !out || (n_pre > 0 && !kv_pre)) return fail(QI21_ERR_ARG, "null pointer");
   AttnArgs a{};
   a.panel = static_cast<const __half*>(panel);
+  a.panel_rows = n_own;
   a.out = static_cast<__half*>(out);
   a.heads = heads;
   a.nseq = 1;

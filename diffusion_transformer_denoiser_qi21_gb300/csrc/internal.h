@@ -71,7 +71,8 @@ struct AttnSeq {
 };
 
 struct AttnArgs {
-  const __half* panel;  // [.][3H]: q at 0, k at H, v at 2H
+  const __half* panel;  // [panel_rows][3H]: q at 0, k at H, v at 2H
+  int panel_rows;
   __half* out;          // [.][H]
   int heads;
   int nseq;
@@ -86,6 +87,7 @@ int sm_count();
 // Each translation unit whose kernels wait on mbarriers keeps its own device
 // status word; these read and clear them (after a device synchronise).
 unsigned int gemm_status_read_clear();
+unsigned int attn_status_read_clear();
 unsigned int read_and_clear_status();
 
 }  // namespace qi21

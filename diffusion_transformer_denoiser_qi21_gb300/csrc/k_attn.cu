@@ -1,300 +1,410 @@
 // Flash attention over [prefix cache, own panel rows] with a leading-run
-// visibility mask (qwen_image21.rs, Qi21Dit::attention + softmax_prefix;
-// gpu_wgpu/qi21.rs, qi_flash): query i of a sequence sees keys
-// [0, lim(i)), lim(i) = vis[i] in the prefill and every key in a step.
-// Keys j < n_pre come from the layer's cache [n_pre][2H] (K then V), the
-// rest from the panel rows [own_row0 + j - n_pre] (K at column H, V at 2H).
+// visibility mask, on the 5th-generation tensor cores (qwen_image21.rs,
+// Qi21Dit::attention + softmax_prefix; gpu_wgpu/qi21.rs, qi_flash).
 //
-// CTA: 8 warps x 16 query rows = 128 queries of one head and one sequence;
-// K/V blocks of 64 keys double-buffered in swizzled shared memory by
-// cp.async (rows past the last key are zero-filled), S = Q K^T and O += P V
-// on the tensor cores (mma.m16n8k16, f16 in, f32 accumulate), the online
-// softmax in f32 registers with exp2 and the 1/sqrt(128) scale folded into
-// the exponent. The key-block loop stops at the visibility of the tile's
-// last live query (vis is non-decreasing); masked keys get weight exactly 0.
-#include <math.h>
+// Query i of a sequence sees keys [0, lim(i)), lim(i) = min(vis[i], keys)
+// in the prefill (block-causal) and every key in a step. Keys j < n_pre
+// come from the layer's cache [n_pre][2H] (K then V), the rest from the
+// panel rows own_row0 + j - n_pre (K at column H, V at 2H).
+//
+// CTA = one 128-query tile of one head of one sequence, 6 warps:
+//   warp 0     TMA: Q once (2 x 64-column boxes, 128-byte swizzle), then K
+//              and V blocks of 128 keys into a 2-stage ring. The cache part
+//              of the key axis is padded to a multiple of 128 so no block
+//              straddles the two sources (padding keys are masked).
+//   warp 1     TMEM allocation and the single MMA-issuing thread:
+//              S_j = Q K_j^T into one of two TMEM buffers (kind::f16, f32
+//              accumulate), then O += P_j V_j with V an MN-major operand.
+//   warps 2-5  softmax: thread t owns query row t (its TMEM lane); reads
+//              S_j with tcgen05.ld, masks, keeps a running max that is only
+//              raised when a block exceeds it by more than 2^8 (then O is
+//              rescaled in TMEM), writes P_j = 2^(s - m) as f16 into
+//              swizzled shared memory (the A operand of P V), accumulates
+//              the row sum; at the end O / l -> f16 rows of the output.
+// The QK^T of block j+1 and the P V of block j-1 run on the tensor cores
+// while the softmax of block j runs on the ALUs. Every wait is bounded.
+#include <algorithm>
+#include <cstdio>
+
+#include <cudaTypedefs.h>
 
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace qi21 {
 
-constexpr int kAttBM = 128;
-constexpr int kAttBN = 64;
-constexpr int kAttD = 128;
-constexpr int kAttThreads = 256;
-constexpr int kAttRowBytes = kAttD * 2;                 // 256 B per row
-constexpr int kAttQBytes = kAttBM * kAttRowBytes;       // 32 KB
-constexpr int kAttKVBytes = kAttBN * kAttRowBytes;      // 16 KB
-constexpr int kAttSmem = kAttQBytes + 4 * kAttKVBytes;  // Q + 2x(K, V) = 96 KB
+static __device__ unsigned int s_attn_status = 0;
 
-// byte offset of 16-byte chunk c (0..15) of row r in a swizzled tile
-__device__ __forceinline__ uint32_t att_swz(int r, int c) {
-  return static_cast<uint32_t>(r * kAttRowBytes + ((c ^ (r & 7)) << 4));
+unsigned int attn_status_read_clear() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, s_attn_status, sizeof v);
+  cudaMemcpyToSymbol(s_attn_status, &z, sizeof z);
+  return v;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int sz = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sz)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+constexpr int kAQ = 128;              // queries per CTA
+constexpr int kAK = 128;              // keys per block
+constexpr int kAD = 128;              // head dim
+constexpr int kSub = 128 * 64 * 2;    // one 128-row x 64-column f16 swizzled box: 16 KB
+constexpr int kTileBytes = 2 * kSub;  // 128 x 128 f16
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;      // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
+constexpr int kOffP = kOffV + 2 * kTileBytes;  // 2 buffers
+constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kAttnSmem = kOffBar + 256 + 1024;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 in f16
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-struct AttnKernelArgs {
-  const __half* panel;
-  __half* out;
-  int heads;
-  int dim;  // H
-  float scale_log2;
-  AttnSeq seq[kMaxSeq];
+struct AttnTcSeq {
+  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 128 (unused if n_pre == 0)
+  const uint32_t* vis;
+  int n_pre, pad_end, q_row0, nq, own_row0, n_own;
 };
 
-__global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(const AttnKernelArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const AttnSeq sq = a.seq[blockIdx.z];
-  const int qt0 = blockIdx.x * kAttBM;
+struct AttnTcParams {
+  CUtensorMap panel;  // [rows][3H] f16, box 64 x 128
+  __half* out;
+  int H;
+  float scale_log2;
+  AttnTcSeq seq[kMaxSeq];
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// key index of virtual key v (cache keys, padding, then own keys), or a
+// value no limit reaches for a padding key
+__device__ __forceinline__ int key_index(int v, int n_pre, int pad_end) {
+  return v < n_pre ? v : (v >= pad_end ? v - pad_end + n_pre : 0x7fffffff);
+}
+
+__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const AttnTcSeq& sq = p.seq[blockIdx.z];
+  const int qt0 = blockIdx.x * kAQ;
   if (qt0 >= sq.nq) return;
   const int h = blockIdx.y;
-  const int H = a.dim;
+  const int H = p.H;
   const int ntot = sq.n_pre + sq.n_own;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int g = lane >> 2;
-  const int tig = lane & 3;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
 
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + kAttQBytes;
-  const uint32_t sV0 = sK0 + 2 * kAttKVBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* qfull = bars + 0;
+  uint64_t* kfull = bars + 1;    // [2]
+  uint64_t* vfull = bars + 3;    // [2]
+  uint64_t* kvempty = bars + 5;  // [2]
+  uint64_t* sfull = bars + 7;    // [2]
+  uint64_t* pfull = bars + 9;    // [2], one per P buffer
+  uint64_t* pvdone = bars + 11;  // [2], one per P buffer
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
-  // Key blocks walked: up to the last live query's visibility.
-  const int q_last = min(qt0 + kAttBM, sq.nq) - 1;
-  const int lim_last = sq.vis ? min(ntot, static_cast<int>(sq.vis[q_last])) : ntot;
-  const int nkb = (lim_last + kAttBN - 1) / kAttBN;
+  // key blocks this tile walks: cache blocks (padded), then own keys up to
+  // the visibility of the tile's last live query (vis is non-decreasing)
+  const int q_last = min(qt0 + kAQ, sq.nq) - 1;
+  const int lim_last = sq.vis ? min(ntot, static_cast<int>(__ldg(sq.vis + q_last))) : ntot;
+  const int own_need = max(0, lim_last - sq.n_pre);
+  const int nkb = sq.pad_end / kAK + (own_need + kAK - 1) / kAK;
 
-  // This thread's two query rows and their limits.
-  const int r0 = qt0 + warp * 16 + g;
-  const int r1 = r0 + 8;
-  const int lim0 = (r0 < sq.nq) ? (sq.vis ? min(ntot, static_cast<int>(sq.vis[r0])) : ntot) : ntot;
-  const int lim1 = (r1 < sq.nq) ? (sq.vis ? min(ntot, static_cast<int>(sq.vis[r1])) : ntot) : ntot;
-
-  const size_t ld_panel = static_cast<size_t>(3) * H;
-  const size_t ld_pre = static_cast<size_t>(2) * H;
-
-  // ---- Q tile -> smem (rows past nq zero-filled)
-  for (int i = tid; i < kAttBM * 16; i += kAttThreads) {
-    const int r = i >> 4, c = i & 15;
-    const int qr = qt0 + r;
-    const bool ok = qr < sq.nq;
-    const __half* src = a.panel + (ok ? (static_cast<size_t>(sq.q_row0 + qr) * ld_panel) : 0) +
-                        h * kAttD + c * 8;
-    cp_async16(sQ + att_swz(r, c), src, ok);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 128 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  auto load_kv = [&](int kb, int buf) {
-    const uint32_t dK = sK0 + buf * kAttKVBytes;
-    const uint32_t dV = sV0 + buf * kAttKVBytes;
-    for (int i = tid; i < kAttBN * 16; i += kAttThreads) {
-      const int r = i >> 4, c = i & 15;
-      const int j = kb * kAttBN + r;
-      const __half* ks;
-      const __half* vs;
-      bool ok = true;
-      if (j < sq.n_pre) {
-        ks = sq.kv_pre + static_cast<size_t>(j) * ld_pre + h * kAttD + c * 8;
-        vs = ks + H;
-      } else if (j < ntot) {
-        const size_t row = static_cast<size_t>(sq.own_row0 + j - sq.n_pre) * ld_panel;
-        ks = a.panel + row + H + h * kAttD + c * 8;
-        vs = ks + H;
-      } else {
-        ks = a.panel;
-        vs = a.panel;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.panel);
+    if (sq.n_pre > 0) tma_prefetch_desc(&sq.kvmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tS = tmem;         // S buffers at columns [0, 256)
+  const uint32_t tO = tmem + 256;   // O at columns [256, 384)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(qfull, kTileBytes);
+      const int qy = sq.q_row0 + qt0;
+      tma_load_2d(smem + kOffQ, &p.panel, qfull, h * kAD, qy);
+      tma_load_2d(smem + kOffQ + kSub, &p.panel, qfull, h * kAD + 64, qy);
+      for (int j = 0; j < nkb; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(&kvempty[s], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) break;
+        uint8_t* kd = smem + kOffK + s * kTileBytes;
+        uint8_t* vd = smem + kOffV + s * kTileBytes;
+        const int v0 = j * kAK;
+        mbar_arrive_expect_tx(&kfull[s], kTileBytes);
+        mbar_arrive_expect_tx(&vfull[s], kTileBytes);
+        if (v0 < sq.n_pre) {
+          tma_load_2d(kd, &sq.kvmap, &kfull[s], h * kAD, v0);
+          tma_load_2d(kd + kSub, &sq.kvmap, &kfull[s], h * kAD + 64, v0);
+          tma_load_2d(vd, &sq.kvmap, &vfull[s], H + h * kAD, v0);
+          tma_load_2d(vd + kSub, &sq.kvmap, &vfull[s], H + h * kAD + 64, v0);
+        } else {
+          const int row = sq.own_row0 + (v0 - sq.pad_end);
+          tma_load_2d(kd, &p.panel, &kfull[s], H + h * kAD, row);
+          tma_load_2d(kd + kSub, &p.panel, &kfull[s], H + h * kAD + 64, row);
+          tma_load_2d(vd, &p.panel, &vfull[s], 2 * H + h * kAD, row);
+          tma_load_2d(vd + kSub, &p.panel, &vfull[s], 2 * H + h * kAD + 64, row);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_f16(128, 128, true);  // V: MN-major
+      const uint32_t sQ = smem_u32(smem + kOffQ);
+      bool ok = mbar_wait(qfull, 0, abort_flag, &s_attn_status);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!mbar_wait(&kfull[s], (j >> 1) & 1, abort_flag, &s_attn_status)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + kOffK + s * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * kSub;
+          tc_mma_f16(tS + (j & 1) * 128, sdesc_sw128(sQ + off) + 2 * (k & 3),
+                     sdesc_sw128(sK + off) + 2 * (k & 3), idesc_qk, k > 0 ? 1u : 0u);
+        }
+        tc_commit(&sfull[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int j = 0; j < nkb && ok; ++j) {
+        if (j + 1 < nkb && !issue_qk(j + 1)) break;
+        const int pb = j & 1;
+        if (!mbar_wait(&pfull[pb], (j >> 1) & 1, abort_flag, &s_attn_status)) break;
+        const int s = j & 1;
+        const uint32_t sP = smem_u32(smem + kOffP + pb * kTileBytes);
+        if (!mbar_wait(&vfull[s], (j >> 1) & 1, abort_flag, &s_attn_status)) break;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + kOffV + s * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          // A = P rows (queries) x 16 keys; B = V: 16 key rows x 128 d,
+          // d contiguous (two 64-wide atoms kSub apart, 8-row groups 1 KB)
+          const uint64_t a = sdesc_sw128(sP + (k >> 2) * kSub) + 2 * (k & 3);
+          const uint64_t b = sdesc(sV + k * 2048, kSub, 1024, 2);
+          tc_mma_f16(tO, a, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&kvempty[s]);
+        tc_commit(&pvdone[pb]);
+      }
+    }
+  } else {
+    // softmax warps: quadrant q of the TMEM lanes = query rows 32q .. 32q+31
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int qi = qt0 + r;
+    const bool live = qi < sq.nq;
+    const int lim = (sq.vis && live) ? min(ntot, static_cast<int>(__ldg(sq.vis + qi))) : lim_last;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const float c = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&sfull[b], (j >> 1) & 1, abort_flag, &s_attn_status)) {
         ok = false;
+        break;
       }
-      cp_async16(dK + att_swz(r, c), ks, ok);
-      cp_async16(dV + att_swz(r, c), vs, ok);
-    }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  uint32_t qf[8][4];
-  float o[16][4];
+      tc_fence_after();
+      uint32_t s[4][32];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  for (int kb = 0; kb < nkb; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < nkb) {
-      load_kv(kb + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (kb == 0) {
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + b * 128 + lane_off + cc * 32, s[cc]);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = 2 * kk + (lane >> 4);
-        ldsm_x4(sQ + att_swz(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-      }
-    }
-    const uint32_t sK = sK0 + buf * kAttKVBytes;
-    const uint32_t sV = sV0 + buf * kAttKVBytes;
-
-    // S = Q K^T: 16 rows x 64 keys per warp
-    float s[8][4];
+      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
+      const int v0 = j * kAK;
+      // every key of this block visible to this row?
+      const int k0 = key_index(v0, sq.n_pre, sq.pad_end);
+      const int k1 = key_index(v0 + kAK - 1, sq.n_pre, sq.pad_end);
+      const bool same_src = (v0 + kAK <= sq.n_pre) || (v0 >= sq.pad_end);
+      const bool all_vis = same_src && k1 < lim && k0 < lim;
+      float mb = -INFINITY;
+      if (all_vis) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = 2 * kk + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sK + att_swz(key, c), b0, b1, b2, b3);
-        mma16816(s[2 * np], qf[kk], b0, b1);
-        mma16816(s[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-
-    // scale, mask, online softmax
-    float mx0 = m0, mx1 = m1;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int key = kb * kAttBN + nt * 8 + 2 * tig;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int kj = key + (e & 1);
-        const int lim = (e < 2) ? lim0 : lim1;
-        const float v = (kj < lim) ? s[nt][e] * a.scale_log2 : -INFINITY;
-        s[nt][e] = v;
-      }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float al0 = exp2f(m0 - mx0);
-    const float al1 = exp2f(m1 - mx1);
-    m0 = mx0;
-    m1 = mx1;
-    float rs0 = 0.f, rs1 = 0.f;
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0 = exp2f(s[nt][0] - mx0);
-      const float p1 = exp2f(s[nt][1] - mx0);
-      const float p2 = exp2f(s[nt][2] - mx1);
-      const float p3 = exp2f(s[nt][3] - mx1);
-      rs0 += p0 + p1;
-      rs1 += p2 + p3;
-      const int kk = nt >> 1;
-      if ((nt & 1) == 0) {
-        pa[kk][0] = pack_half2(p0, p1);
-        pa[kk][1] = pack_half2(p2, p3);
+          for (int e = 0; e < 32; ++e) mb = fmaxf(mb, __uint_as_float(s[cc][e]));
       } else {
-        pa[kk][2] = pack_half2(p0, p1);
-        pa[kk][3] = pack_half2(p2, p3);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int kj = key_index(v0 + cc * 32 + e, sq.n_pre, sq.pad_end);
+            const float x = (kj < lim) ? __uint_as_float(s[cc][e]) : -INFINITY;
+            s[cc][e] = __float_as_uint(x);
+            mb = fmaxf(mb, x);
+          }
+      }
+      mb *= c;
+      // raise the running max only past the threshold (exact: O and l share
+      // the stale max; P <= 2^threshold stays in f16 range)
+      float alpha = 1.f;
+      const bool need = mb > m + kRescaleThreshold;
+      if (need) {
+        alpha = ex2(m - mb);
+        m = mb;
+        l *= alpha;
+      }
+      const bool warp_rescale = __any_sync(0xffffffffu, need && j > 0);
+      if (j >= 2) {
+        // P buffer b was last read by the P V of block j - 2
+        if (!mbar_wait(&pvdone[b], ((j - 2) >> 1) & 1, abort_flag, &s_attn_status)) {
+          ok = false;
+          break;
+        }
+      }
+      // P row -> swizzled K-major smem (two 64-key halves of 128 B per row)
+      uint8_t* prow = smem + kOffP + b * kTileBytes + r * 128;
+      float rs = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = ch * 8 + 2 * e;
+          const float p0 = ex2(fmaf(__uint_as_float(s[k >> 5][k & 31]), c, -m));
+          const float p1 = ex2(fmaf(__uint_as_float(s[k >> 5][(k & 31) + 1]), c, -m));
+          rs += p0 + p1;
+          w4[e] = pack_half2(p0, p1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(prow + (ch >> 3) * kSub + (((ch & 7) ^ (r & 7)) << 4));
+        *dst = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      l += rs;
+      fence_async_smem();
+      if (warp_rescale) {
+        // O is stable once the P V of block j - 1 is done
+        if (!mbar_wait(&pvdone[b ^ 1], ((j - 1) >> 1) & 1, abort_flag, &s_attn_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + lane_off + cc * 32, o);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&pfull[b]);
+    }
+    if (ok && mbar_wait(&pvdone[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, abort_flag, &s_attn_status)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __half* orow = p.out + static_cast<size_t>(sq.q_row0 + qi) * H + h * kAD;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + lane_off + cc * 32, o);
+        tmem_ld_wait(o);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            dst[g] = make_uint4(
+                pack_half2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv),
+                pack_half2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv),
+                pack_half2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv),
+                pack_half2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv));
+        }
       }
     }
-    l0 = l0 * al0 + rs0;
-    l1 = l1 * al1 + rs1;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      o[dt][0] *= al0;
-      o[dt][1] *= al0;
-      o[dt][2] *= al1;
-      o[dt][3] *= al1;
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int c = 2 * dp + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sV + att_swz(key, c), b0, b1, b2, b3);
-        mma16816(o[2 * dp], pa[kk], b0, b1);
-        mma16816(o[2 * dp + 1], pa[kk], b2, b3);
-      }
-    }
-    __syncthreads();
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
 
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float i0 = 1.f / l0;
-  const float i1 = 1.f / l1;
-  __half* out0 = a.out + static_cast<size_t>(sq.q_row0 + r0) * H + h * kAttD + 2 * tig;
-  __half* out1 = a.out + static_cast<size_t>(sq.q_row0 + r1) * H + h * kAttD + 2 * tig;
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt) {
-    if (r0 < sq.nq)
-      *reinterpret_cast<uint32_t*>(out0 + dt * 8) = pack_half2(o[dt][0] * i0, o[dt][1] * i0);
-    if (r1 < sq.nq)
-      *reinterpret_cast<uint32_t*>(out1 + dt * 8) = pack_half2(o[dt][2] * i1, o[dt][3] * i1);
+// ---------------------------------------------------------------- host ----
+
+static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   }
+  return fn;
+}
+
+static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  auto fn = attn_encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAttSmem);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kAttnSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  AttnKernelArgs a;
-  a.panel = in.panel;
-  a.out = in.out;
-  a.heads = in.heads;
-  a.dim = in.heads * kAttD;
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kAttD)));
+  AttnTcParams prm;
+  memset(&prm, 0, sizeof prm);
+  const int H = in.heads * kAD;
+  prm.out = in.out;
+  prm.H = H;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kAD)));
+  cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows);
+  if (e != cudaSuccess) return e;
   int maxq = 0;
   for (int i = 0; i < in.nseq; ++i) {
-    a.seq[i] = in.seq[i];
-    maxq = maxq > in.seq[i].nq ? maxq : in.seq[i].nq;
+    const AttnSeq& a = in.seq[i];
+    AttnTcSeq& t = prm.seq[i];
+    t.vis = a.vis;
+    t.n_pre = a.n_pre;
+    t.pad_end = (a.n_pre + kAK - 1) / kAK * kAK;
+    t.q_row0 = a.q_row0;
+    t.nq = a.nq;
+    t.own_row0 = a.own_row0;
+    t.n_own = a.n_own;
+    if (a.n_pre > 0) {
+      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre);
+      if (e != cudaSuccess) return e;
+    }
+    maxq = std::max(maxq, a.nq);
   }
-  for (int i = in.nseq; i < kMaxSeq; ++i) a.seq[i] = AttnSeq{};
   if (maxq == 0) return cudaSuccess;
-  dim3 grid((maxq + kAttBM - 1) / kAttBM, in.heads, in.nseq);
-  attn_mma_kernel<<<grid, kAttThreads, kAttSmem, s>>>(a);
+  dim3 grid((maxq + kAQ - 1) / kAQ, in.heads, in.nseq);
+  attn_tc_kernel<<<grid, 192, kAttnSmem, s>>>(prm);
   return cudaGetLastError();
 }
 
