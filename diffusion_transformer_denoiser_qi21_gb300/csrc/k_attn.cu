@@ -7,7 +7,7 @@
 // come from the layer's cache [n_pre][2H] (K then V), the rest from the
 // panel rows own_row0 + j - n_pre (K at column H, V at 2H).
 //
-// CTA = one 128-query tile of one head of one sequence, 6 warps:
+// CTA = one 128-query tile of one head of one sequence, 10 warps:
 //   warp 0     TMA: Q once (2 x 64-column boxes, 128-byte swizzle), then K
 //              and V blocks of 128 keys into a 2-stage ring. The cache part
 //              of the key axis is padded to a multiple of 128 so no block
@@ -15,12 +15,15 @@
 //   warp 1     TMEM allocation and the single MMA-issuing thread:
 //              S_j = Q K_j^T into one of two TMEM buffers (kind::f16, f32
 //              accumulate), then O += P_j V_j with V an MN-major operand.
-//   warps 2-5  softmax: thread t owns query row t (its TMEM lane); reads
-//              S_j with tcgen05.ld, masks, keeps a running max that is only
-//              raised when a block exceeds it by more than 2^8 (then O is
-//              rescaled in TMEM), writes P_j = 2^(s - m) as f16 into
-//              swizzled shared memory (the A operand of P V), accumulates
-//              the row sum; at the end O / l -> f16 rows of the output.
+//   warps 2-9  softmax: two warps per TMEM lane quadrant, each owning 64 of
+//              the 128 key columns of its 32 query rows. Per block: read S_j
+//              with tcgen05.ld, mask, exchange the partial row max with the
+//              partner warp (shared memory + a 64-thread named barrier), keep
+//              a running max that is only raised when a block exceeds it by
+//              more than 2^8 (then O is rescaled in TMEM), write
+//              P_j = 2^(s - m) as f16 into swizzled shared memory (the A
+//              operand of P V) and accumulate the row sum; at the end
+//              O / l -> f16 rows of the output.
 // The QK^T of block j+1 and the P V of block j-1 run on the tensor cores
 // while the softmax of block j runs on the ALUs. Every wait is bounded.
 #include <algorithm>
@@ -52,7 +55,9 @@ constexpr int kOffK = kOffQ + kTileBytes;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
 constexpr int kOffP = kOffV + 2 * kTileBytes;  // 2 buffers
 constexpr int kOffBar = kOffP + 2 * kTileBytes;
-constexpr int kAttnSmem = kOffBar + 256 + 1024;
+constexpr int kOffX = kOffBar + 256;        // partial row max / sum exchange [2][128] f32
+constexpr int kAttnSmem = kOffX + 1024 + 1024;
+constexpr int kAttnThreads = 320;           // 10 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 in f16
 
 struct AttnTcSeq {
@@ -75,6 +80,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -85,7 +119,7 @@ __device__ __forceinline__ int key_index(int v, int n_pre, int pad_end) {
   return v < n_pre ? v : (v >= pad_end ? v - pad_end + n_pre : 0x7fffffff);
 }
 
-__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -102,11 +136,13 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   uint64_t* qfull = bars + 0;
   uint64_t* kfull = bars + 1;    // [2]
   uint64_t* vfull = bars + 3;    // [2]
-  uint64_t* kvempty = bars + 5;  // [2]
-  uint64_t* sfull = bars + 7;    // [2]
-  uint64_t* pfull = bars + 9;    // [2], one per P buffer
-  uint64_t* pvdone = bars + 11;  // [2], one per P buffer
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* kempty = bars + 5;   // [2] K stage free (its QK^T done)
+  uint64_t* vempty = bars + 7;   // [2] V stage free (its P V done)
+  uint64_t* sfull = bars + 9;    // [2]
+  uint64_t* pfull = bars + 11;   // [2], one per P buffer
+  uint64_t* pvdone = bars + 13;  // [2], one per P buffer
+  uint64_t* xbar = bars + 15;    // [4], the two softmax warps of a lane quadrant
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   // key blocks this tile walks: cache blocks (padded), then own keys up to
@@ -117,7 +153,8 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   const int nkb = sq.pad_end / kAK + (own_need + kAK - 1) / kAK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 128 : 1);
+    for (int i = 0; i < 15; ++i) mbar_init(&bars[i], (i == 11 || i == 12) ? 256 : 1);
+    for (int i = 15; i < 19; ++i) mbar_init(&bars[i], 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -142,26 +179,43 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       const int qy = sq.q_row0 + qt0;
       tma_load_2d(smem + kOffQ, &p.panel, qfull, h * kAD, qy);
       tma_load_2d(smem + kOffQ + kSub, &p.panel, qfull, h * kAD + 64, qy);
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kvempty[s], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) break;
-        uint8_t* kd = smem + kOffK + s * kTileBytes;
-        uint8_t* vd = smem + kOffV + s * kTileBytes;
+      // need order: K_{j+1} (for QK^T one block ahead), then V_j (for P V)
+      auto load_k = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&kempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
+        uint8_t* kd = smem + kOffK + st * kTileBytes;
         const int v0 = j * kAK;
-        mbar_arrive_expect_tx(&kfull[s], kTileBytes);
-        mbar_arrive_expect_tx(&vfull[s], kTileBytes);
+        mbar_arrive_expect_tx(&kfull[st], kTileBytes);
         if (v0 < sq.n_pre) {
-          tma_load_2d(kd, &sq.kvmap, &kfull[s], h * kAD, v0);
-          tma_load_2d(kd + kSub, &sq.kvmap, &kfull[s], h * kAD + 64, v0);
-          tma_load_2d(vd, &sq.kvmap, &vfull[s], H + h * kAD, v0);
-          tma_load_2d(vd + kSub, &sq.kvmap, &vfull[s], H + h * kAD + 64, v0);
+          tma_load_2d(kd, &sq.kvmap, &kfull[st], h * kAD, v0);
+          tma_load_2d(kd + kSub, &sq.kvmap, &kfull[st], h * kAD + 64, v0);
         } else {
           const int row = sq.own_row0 + (v0 - sq.pad_end);
-          tma_load_2d(kd, &p.panel, &kfull[s], H + h * kAD, row);
-          tma_load_2d(kd + kSub, &p.panel, &kfull[s], H + h * kAD + 64, row);
-          tma_load_2d(vd, &p.panel, &vfull[s], 2 * H + h * kAD, row);
-          tma_load_2d(vd + kSub, &p.panel, &vfull[s], 2 * H + h * kAD + 64, row);
+          tma_load_2d(kd, &p.panel, &kfull[st], H + h * kAD, row);
+          tma_load_2d(kd + kSub, &p.panel, &kfull[st], H + h * kAD + 64, row);
         }
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&vempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
+        uint8_t* vd = smem + kOffV + st * kTileBytes;
+        const int v0 = j * kAK;
+        mbar_arrive_expect_tx(&vfull[st], kTileBytes);
+        if (v0 < sq.n_pre) {
+          tma_load_2d(vd, &sq.kvmap, &vfull[st], H + h * kAD, v0);
+          tma_load_2d(vd + kSub, &sq.kvmap, &vfull[st], H + h * kAD + 64, v0);
+        } else {
+          const int row = sq.own_row0 + (v0 - sq.pad_end);
+          tma_load_2d(vd, &p.panel, &vfull[st], 2 * H + h * kAD, row);
+          tma_load_2d(vd + kSub, &p.panel, &vfull[st], 2 * H + h * kAD + 64, row);
+        }
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; j < nkb && ok; ++j) {
+        if (j + 1 < nkb && !load_k(j + 1)) break;
+        ok = load_v(j);
       }
     }
   } else if (warp == 1) {
@@ -181,6 +235,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           tc_mma_f16(tS + (j & 1) * 128, sdesc_sw128(sQ + off) + 2 * (k & 3),
                      sdesc_sw128(sK + off) + 2 * (k & 3), idesc_qk, k > 0 ? 1u : 0u);
         }
+        tc_commit(&kempty[s]);
         tc_commit(&sfull[j & 1]);
         return true;
       };
@@ -202,21 +257,33 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           const uint64_t b = sdesc(sV + k * 2048, kSub, 1024, 2);
           tc_mma_f16(tO, a, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(&kvempty[s]);
+        tc_commit(&vempty[s]);
         tc_commit(&pvdone[pb]);
       }
     }
   } else {
-    // softmax warps: quadrant q of the TMEM lanes = query rows 32q .. 32q+31
+    // softmax warps: quadrant q of the TMEM lanes = query rows 32q .. 32q+31,
+    // half hf = key columns [64 hf, 64 hf + 64) of every block
     const int q = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const int qi = qt0 + r;
     const bool live = qi < sq.nq;
     const int lim = (sq.vis && live) ? min(ntot, static_cast<int>(__ldg(sq.vis + qi))) : lim_last;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + kOffX);  // [2][128]
     const float c = p.scale_log2;
+    const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // bounded rendezvous of the two warps of this quadrant
+    uint32_t xph = 0;
+    auto pair_sync = [&]() -> bool {
+      mbar_arrive(&xbar[q]);
+      const bool r_ok = mbar_wait(&xbar[q], xph, abort_flag, &s_attn_status);
+      xph ^= 1u;
+      return r_ok;
+    };
     for (int j = 0; j < nkb; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&sfull[b], (j >> 1) & 1, abort_flag, &s_attn_status)) {
@@ -224,35 +291,48 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         break;
       }
       tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + b * 128 + lane_off + cc * 32, s[cc]);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
-      const int v0 = j * kAK;
-      // every key of this block visible to this row?
+      uint32_t s[2][32];
+      tmem_ld32(tS + b * 128 + lane_off + hf * 64, s[0]);
+      tmem_ld32(tS + b * 128 + lane_off + hf * 64 + 32, s[1]);
+      tmem_ld_wait(s[0]);
+      tmem_ld_wait(s[1]);
+      const int v0 = j * kAK + hf * 64;
+      // every key of this half-block visible to this row?
       const int k0 = key_index(v0, sq.n_pre, sq.pad_end);
-      const int k1 = key_index(v0 + kAK - 1, sq.n_pre, sq.pad_end);
-      const bool same_src = (v0 + kAK <= sq.n_pre) || (v0 >= sq.pad_end);
-      const bool all_vis = same_src && k1 < lim && k0 < lim;
-      float mb = -INFINITY;
-      if (all_vis) {
+      const int k1 = key_index(v0 + 63, sq.n_pre, sq.pad_end);
+      const bool same_src = (v0 + 64 <= sq.n_pre) || (v0 >= sq.pad_end);
+      if (!(same_src && k1 < lim && k0 < lim)) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mb = fmaxf(mb, __uint_as_float(s[cc][e]));
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int kj = key_index(v0 + cc * 32 + e, sq.n_pre, sq.pad_end);
-            const float x = (kj < lim) ? __uint_as_float(s[cc][e]) : -INFINITY;
-            s[cc][e] = __float_as_uint(x);
-            mb = fmaxf(mb, x);
+            if (kj >= lim) s[cc][e] = __float_as_uint(-INFINITY);
           }
       }
-      mb *= c;
+      float mx[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) mx[a] = __uint_as_float(s[a >> 1][(a & 1) * 16]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 1; e < 15; e += 2)
+          mx[a] = max3(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + e]),
+                       __uint_as_float(s[a >> 1][(a & 1) * 16 + e + 1]));
+#pragma unroll
+      for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + 15]));
+      const float pmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      xch[hf * 128 + r] = pmax;
+      if (!pair_sync()) {
+        ok = false;
+        break;
+      }
+      const float omax = xch[(hf ^ 1) * 128 + r];
+      if (!pair_sync()) {
+        ok = false;
+        break;
+      }
+      const float mb = fmaxf(pmax, omax) * c;
       // raise the running max only past the threshold (exact: O and l share
       // the stale max; P <= 2^threshold stays in f16 range)
       float alpha = 1.f;
@@ -270,24 +350,33 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           break;
         }
       }
-      // P row -> swizzled K-major smem (two 64-key halves of 128 B per row)
-      uint8_t* prow = smem + kOffP + b * kTileBytes + r * 128;
-      float rs = 0.f;
+      // this half of the P row -> swizzled K-major smem (64 keys = 128 B)
+      uint8_t* prow = smem + kOffP + b * kTileBytes + hf * kSub + r * 128;
+      const uint64_t nm2 = f2(-m, -m);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < 8; ++ch) {
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int k = ch * 8 + 2 * e;
-          const float p0 = ex2(fmaf(__uint_as_float(s[k >> 5][k & 31]), c, -m));
-          const float p1 = ex2(fmaf(__uint_as_float(s[k >> 5][(k & 31) + 1]), c, -m));
-          rs += p0 + p1;
+          const uint64_t x = ffma2(f2(__uint_as_float(s[k >> 5][k & 31]), __uint_as_float(s[k >> 5][(k & 31) + 1])),
+                                   c2, nm2);
+          float x0, x1;
+          unf2(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc[e] = fadd2(acc[e], f2(p0, p1));
           w4[e] = pack_half2(p0, p1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(prow + (ch >> 3) * kSub + (((ch & 7) ^ (r & 7)) << 4));
+        uint4* dst = reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4));
         *dst = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      l += rs;
+      {
+        const uint64_t t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+        float t0, t1;
+        unf2(t, t0, t1);
+        l += t0 + t1;
+      }
       fence_async_smem();
       if (warp_rescale) {
         // O is stable once the P V of block j - 1 is done
@@ -297,13 +386,13 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tO + lane_off + cc * 32, o);
+          tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + lane_off + cc * 32, o);
+          tmem_st32(tO + lane_off + hf * 64 + cc * 32, o);
         }
         tmem_st_wait();
       }
@@ -312,12 +401,14 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     }
     if (ok && mbar_wait(&pvdone[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, abort_flag, &s_attn_status)) {
       tc_fence_after();
-      const float inv = 1.f / l;
-      __half* orow = p.out + static_cast<size_t>(sq.q_row0 + qi) * H + h * kAD;
+      xch[hf * 128 + r] = l;
+      pair_sync();
+      const float inv = 1.f / (l + xch[(hf ^ 1) * 128 + r]);
+      __half* orow = p.out + static_cast<size_t>(sq.q_row0 + qi) * H + h * kAD + hf * 64;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + cc * 32, o);
+        tmem_ld32(tO + lane_off + hf * 64 + cc * 32, o);
         tmem_ld_wait(o);
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
@@ -404,7 +495,7 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
   }
   if (maxq == 0) return cudaSuccess;
   dim3 grid((maxq + kAQ - 1) / kAQ, in.heads, in.nseq);
-  attn_tc_kernel<<<grid, 192, kAttnSmem, s>>>(prm);
+  attn_tc_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(prm);
   return cudaGetLastError();
 }
 
