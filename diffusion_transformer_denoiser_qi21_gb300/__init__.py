@@ -17,7 +17,7 @@ from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_T
 
 __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
-    "workspace_bytes", "pack_layer", "prefill", "step", "step_batch", "device_status", "build",
+    "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -155,6 +155,15 @@ def step(g: Geom, layers, cache: KVCache, x_in, x_out, mods, workspace, x_layers
                            _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _ptr(x_layers, f, "x_layers"),
                            _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
                            _stream(stream)))
+
+
+def step_noalloc(g: Geom, layers, cache: KVCache, x_in, x_out, mods, stream=None):
+    """qi21_step_noalloc: the step with the library's static device scratch
+    instead of a caller workspace (for callers that cannot allocate)."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_step_noalloc(C.byref(g), _layer_array(layers), cache.handle, _ptr(x_in, f, "x_in"),
+                                   _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _stream(stream)))
 
 
 def step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace, x_layers=None, stream=None):

@@ -72,6 +72,7 @@ _SIGS = {
     "qi21_step": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "qi21_step_batch": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), C.POINTER(_vp), _i32, _vp, _vp, _vp,
                                   _vp, _vp, _sz, _vp]),
+    "qi21_step_noalloc": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp]),
     "qi21_device_status": (C.c_int, []),
     "qi21_profile_enable": (C.c_int, [C.c_int]),
     "qi21_profile_read": (C.c_int, [_vp, _vp]),

@@ -31,6 +31,8 @@ static int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 static int cuda_fail(cudaError_t e, const char* what) {
   return fail(e == cudaErrorMemoryAllocation ? QI21_ERR_OOM : QI21_ERR_CUDA, "%s: %s", what,
               cudaGetErrorString(e));
@@ -78,6 +80,8 @@ static cudaEvent_t prof_event() {
   }
   return g_prof_pool[g_prof_used++];
 }
+
+bool profiling_on() { return g_prof_on; }
 
 class ProfScope {
  public:

@@ -84,6 +84,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 // --------------------------------------------------------------- device ----
 
 int sm_count();
+// Sets the thread-local error text of qi21_last_error and returns code.
+int report_error(int code, const char* msg);
+// True while qi21_profile_enable(1) is in force (launches create events).
+bool profiling_on();
 // Each translation unit whose kernels wait on mbarriers keeps its own device
 // status word; these read and clear them (after a device synchronise).
 unsigned int gemm_status_read_clear();

@@ -196,6 +196,32 @@ int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* 
               const float* x_in, float* x_out, const float* mods, float* x_layers,
               void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the static device scratch behind qi21_step_noalloc: 32 MiB,
+ * i.e. qi21_workspace_bytes(g, n) <= this bound (dim 4096 / mlp 12288: up to
+ * 408 target rows; dim 256 / mlp 768: up to 6552). */
+#define QI21_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* qi21_step without a caller workspace, for callers that cannot allocate
+ * device memory: hosts whose device memory belongs to another allocator and
+ * who have no buffer to lend, or serving loops under a no-allocation rule
+ * after start-up (cudaMalloc may synchronise the device and stall every
+ * other stream). The page has no counterpart; this is a library addition.
+ * Same arguments and results as qi21_step without x_layers and workspace:
+ * the workspace is a file-scope static device array of
+ * QI21_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits. The entry point allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine); it returns QI21_ERR_WORKSPACE
+ * when qi21_workspace_bytes(g, n) exceeds the scratch and QI21_ERR_STATE
+ * while qi21_profile_enable(1) is on (profiling creates CUDA events).
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. All calls share the one scratch and it keeps
+ * the last call's contents (nothing in it needs to start at zero: the step
+ * writes every scratch byte it reads), so calls that overlap on the GPU --
+ * concurrent streams, or two host threads -- race: serialise them. */
+int qi21_step_noalloc(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache,
+                      const float* x_in, float* x_out, const float* mods, void* stream);
+
 /* Step of `nseq` (1..8) sequences that share the weights, the modulation
  * and the target row count n (a classifier-free-guidance pair: one latent,
  * two prompts). Sequence s has its own cache caches[s] (own prefix, own
