@@ -85,6 +85,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ------------------------------------------------------------ replicas --
+
+def aggregate(elapsed_s, rows_per_step, steps, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: every rank processed
+    rows_per_step x steps rows; the job took the slowest rank's time.
+    Returns (max elapsed seconds over ranks, rows/s over all ranks)."""
+    import torch
+    world = 1
+    t = torch.tensor([float(elapsed_s)], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        world = dist.get_world_size()
+    t_max = float(t.item())
+    return t_max, rows_per_step * steps * world / t_max
+
+
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -146,52 +162,57 @@ class ClockSampler:
 
 # ---------------------------------------------------------- CPU baseline --
 
-def oracle_layer_sample(w, r, reps=1):
-    """Time the oracle on layer 0 of the step: the keys/values of all n
-    target rows (against the layer-0 prefix cache) plus the query side of
-    the first r target rows, each part timed, scaled to n rows and L layers.
-    Returns (rows_per_s, seconds_measured, description)."""
-    import numpy as np
+class OracleSample:
+    """The oracle on layer 0 of the step, as a bounded sample of the
+    workload: the keys/values of all n target rows (against the layer-0
+    prefix cache, computed once, untimed) plus the query side (q, attention,
+    O, FFN) of r target rows; each part timed and scaled to n rows and L
+    layers."""
 
-    from oracle import qi21_oracle as O
-    from synthetic import qi21_inputs as S
+    def __init__(self, w):
+        from oracle import qi21_oracle as O
+        from synthetic import qi21_inputs as S
+        self.O, self.w = O, w
+        self.cfg = O.cfg_of(w)
+        segs = w.segs(0)
+        self.lp = O.prefix_len(segs)
+        self.W = S.layer_weights(w, 0)
+        cp, sp = O.rope_tables(O.positions(segs)[:self.lp], self.cfg["axes"], self.cfg["theta"])
+        vis = O.prefix_visibility(segs)
+        _, self.kp, self.vp = O.block(S.x_prefix(w, 0), self.W, S.mods0(w), cp, sp, self.cfg, None, vis,
+                                      rows=[0])
+        self.ct, self.st = O.target_rope(segs, self.cfg["axes"], self.cfg["theta"])
+        self.x = S.x_target(w)
+        self.m = S.mods_t(w)
 
-    cfg = O.cfg_of(w)
-    segs = w.segs(0)
-    lp = O.prefix_len(segs)
-    W = S.layer_weights(w, 0)
-    cp, sp = O.rope_tables(O.positions(segs)[:lp], cfg["axes"], cfg["theta"])
-    vis = O.prefix_visibility(segs)
-    # the layer-0 prefix cache (untimed): K/V of every prefix row
-    _, kp, vp = O.block(S.x_prefix(w, 0), W, S.mods0(w), cp, sp, cfg, None, vis, rows=[0])
-    ct, st = O.target_rope(segs, cfg["axes"], cfg["theta"])
-    x = S.x_target(w)
-    m = S.mods_t(w)
-    n = w.n_target
-    r = n if r <= 0 else min(r, n)
-    best = None
-    spent = 0.0
-    for _ in range(reps):
+    def layer_seconds(self, r):
+        """(estimated seconds of one full layer on all n rows, seconds spent)."""
+        import numpy as np
+        O, n = self.O, self.w.n_target
+        r = n if r <= 0 else min(r, n)
         t0 = time.perf_counter()
-        O.block(x, W, m, ct, st, cfg, (kp, vp), None, rows=np.arange(r))
+        O.block(self.x, self.W, self.m, self.ct, self.st, self.cfg, (self.kp, self.vp), None, rows=np.arange(r))
         t1 = time.perf_counter()
-        t_all = t1 - t0
-        if r < n:
-            # the key/value side alone (query side restricted to one row)
-            O.block(x, W, m, ct, st, cfg, (kp, vp), None, rows=[0])
-            t2 = time.perf_counter()
-            t_kv = t2 - t1
-            t_layer = t_kv + (t_all - t_kv) * (n / r)
-            spent += t2 - t0
-        else:
-            t_layer = t_all
-            spent += t_all
-        best = t_layer if best is None else min(best, t_layer)
-    rows_per_s = n / (best * w.layers)
-    desc = (f"oracle (numpy float64, BLAS matmuls) on layer 0 of {w.layers}: K/V of all {n} target "
-            f"rows against the {lp}-row layer-0 cache + the query side of {r} of {n} rows; time "
-            f"scaled to {n} rows x {w.layers} layers")
-    return rows_per_s, spent, desc
+        if r == n:
+            return t1 - t0, t1 - t0
+        O.block(self.x, self.W, self.m, self.ct, self.st, self.cfg, (self.kp, self.vp), None, rows=[0])
+        t2 = time.perf_counter()
+        t_kv = t2 - t1
+        return t_kv + ((t1 - t0) - t_kv) * (n / r), t2 - t0
+
+    def describe(self, r):
+        n, L = self.w.n_target, self.w.layers
+        r = n if r <= 0 else min(r, n)
+        return (f"oracle (numpy float64, BLAS matmuls) on layer 0 of {L}: K/V of all {n} target rows "
+                f"against the {self.lp}-row layer-0 cache + the query side of {r} of {n} rows; "
+                f"time scaled to {n} rows x {L} layers")
+
+
+def oracle_layer_sample(w, r):
+    """(rows/s, seconds spent, description) of one timed oracle sample."""
+    smp = OracleSample(w)
+    t_layer, spent = smp.layer_seconds(r)
+    return w.n_target / (t_layer * w.layers), spent, smp.describe(r)
 
 
 def cpu_cores():
@@ -211,12 +232,13 @@ def run_reference(args):
     from synthetic import qi21_inputs as S
     w = S.WORKLOADS[args.workload]
     r = args.cpu_rows if args.cpu_rows > 0 else 128
+    smp = OracleSample(w)
+    desc = smp.describe(r)
     times = []
-    desc = ""
     for i in range(args.warmup + args.steps):
-        rps, spent, desc = oracle_layer_sample(w, r)
+        t_layer, _ = smp.layer_seconds(r)
         if i >= args.warmup:
-            times.append(w.n_target / rps / w.layers)  # estimated seconds per layer
+            times.append(t_layer)
     t_layer = statistics.median(times)
     value = w.n_target / (t_layer * w.layers)
     ms = t_layer * w.layers * 1e3
@@ -324,12 +346,9 @@ def run_gpu(args):
     launches = {k: launches1[k] - launches0[k] for k in launches1}
     gpu_launches = int(sum(launches.values()))
 
-    t_max = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    t_max_ms = float(t_max.item())
-    value = n_rows * args.steps * world / (t_max_ms * 1e-3)
-    tflops = flops_step * args.steps * world / (t_max_ms * 1e-3) / 1e12
+    t_max_s, value = aggregate(elapsed_ms * 1e-3, n_rows, args.steps, dist, device="cuda")
+    t_max_ms = t_max_s * 1e3
+    tflops = flops_step * args.steps * world / t_max_s / 1e12
 
     # end to end through host buffers: pinned x in, x out back each step
     e2e = None
@@ -349,11 +368,9 @@ def run_gpu(args):
             out_host.copy_(dw.x_out, non_blocking=True)
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device="cuda")
-        if dist is not None:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        _, e2e_value = aggregate(t_e2e, n_rows, args.steps, dist, device="cuda")
         h2d = x_host.numel() * 4 + m_host.numel() * 4
-        e2e = {"value": n_rows * args.steps * world / float(tt.item()), "unit": UNIT,
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_host.numel() * 4)}
 
     peaks, peak_src = load_peaks()
