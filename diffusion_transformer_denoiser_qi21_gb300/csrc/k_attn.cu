@@ -14,16 +14,17 @@
 //              straddles the two sources (padding keys are masked).
 //   warp 1     TMEM allocation and the single MMA-issuing thread:
 //              S_j = Q K_j^T into one of two TMEM buffers (kind::f16, f32
-//              accumulate), then O += P_j V_j with V an MN-major operand.
+//              accumulate), then O += P_j V_j with P read from TMEM and V an
+//              MN-major shared-memory operand.
 //   warps 2-9  softmax: two warps per TMEM lane quadrant, each owning 64 of
 //              the 128 key columns of its 32 query rows. Per block: read S_j
 //              with tcgen05.ld, mask, exchange the partial row max with the
 //              partner warp (shared memory + a 64-thread named barrier), keep
 //              a running max that is only raised when a block exceeds it by
 //              more than 2^8 (then O is rescaled in TMEM), write
-//              P_j = 2^(s - m) as f16 into swizzled shared memory (the A
-//              operand of P V) and accumulate the row sum; at the end
-//              O / l -> f16 rows of the output.
+//              P_j = 2^(s - m) as packed f16 pairs into TMEM (the A operand
+//              of P V, one of two P buffers) and accumulate the row sum; at
+//              the end O / l -> f16 rows of the output.
 // The QK^T of block j+1 and the P V of block j-1 run on the tensor cores
 // while the softmax of block j runs on the ALUs. Every wait is bounded.
 #include <algorithm>
@@ -53,8 +54,7 @@ constexpr int kTileBytes = 2 * kSub;  // 128 x 128 f16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
-constexpr int kOffP = kOffV + 2 * kTileBytes;  // 2 buffers
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kOffBar = kOffV + 2 * kTileBytes;
 constexpr int kOffX = kOffBar + 256;        // partial row max / sum exchange [2][128] f32
 constexpr int kAttnSmem = kOffX + 1024 + 1024;
 constexpr int kAttnThreads = 320;           // 10 warps
@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   const uint32_t tmem = *tslot;
   const uint32_t tS = tmem;         // S buffers at columns [0, 256)
   const uint32_t tO = tmem + 256;   // O at columns [256, 384)
+  const uint32_t tP = tmem + 384;   // P buffers (f16 pairs) at [384, 448), [448, 512)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -245,17 +246,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
         const int pb = j & 1;
         if (!mbar_wait(&pfull[pb], (j >> 1) & 1, abort_flag, &s_attn_status)) break;
         const int s = j & 1;
-        const uint32_t sP = smem_u32(smem + kOffP + pb * kTileBytes);
         if (!mbar_wait(&vfull[s], (j >> 1) & 1, abort_flag, &s_attn_status)) break;
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + kOffV + s * kTileBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          // A = P rows (queries) x 16 keys; B = V: 16 key rows x 128 d,
-          // d contiguous (two 64-wide atoms kSub apart, 8-row groups 1 KB)
-          const uint64_t a = sdesc_sw128(sP + (k >> 2) * kSub) + 2 * (k & 3);
+          // A = P in TMEM: 128 query lanes x 16 keys = 8 columns of f16
+          // pairs; B = V: 16 key rows x 128 d, d contiguous (two 64-wide
+          // atoms kSub apart, 8-row groups 1 KB)
           const uint64_t b = sdesc(sV + k * 2048, kSub, 1024, 2);
-          tc_mma_f16(tO, a, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tO, tP + pb * 64 + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&vempty[s]);
         tc_commit(&pvdone[pb]);
@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 #pragma unroll
       for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + 15]));
       const float pmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      // the partner warp holds the other 64 columns of these rows
       xch[hf * 128 + r] = pmax;
       if (!pair_sync()) {
         ok = false;
@@ -350,34 +351,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
           break;
         }
       }
-      // this half of the P row -> swizzled K-major smem (64 keys = 128 B)
-      uint8_t* prow = smem + kOffP + b * kTileBytes + hf * kSub + r * 128;
+      // this half of the P row -> TMEM: 64 keys = 32 columns of f16 pairs
       const uint64_t nm2 = f2(-m, -m);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = ch * 8 + 2 * e;
-          const uint64_t x = ffma2(f2(__uint_as_float(s[k >> 5][k & 31]), __uint_as_float(s[k >> 5][(k & 31) + 1])),
-                                   c2, nm2);
-          float x0, x1;
-          unf2(x, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          acc[e] = fadd2(acc[e], f2(p0, p1));
-          w4[e] = pack_half2(p0, p1);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4));
-        *dst = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      for (int i = 0; i < 32; ++i) {
+        const int k = 2 * i;
+        const uint64_t x = ffma2(f2(__uint_as_float(s[k >> 5][k & 31]), __uint_as_float(s[k >> 5][(k & 31) + 1])),
+                                 c2, nm2);
+        float x0, x1;
+        unf2(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        acc[i & 3] = fadd2(acc[i & 3], f2(p0, p1));
+        pk[i] = pack_half2(p0, p1);
       }
+      tmem_st32(tP + b * 64 + hf * 32 + lane_off, pk);
       {
         const uint64_t t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
         float t0, t1;
         unf2(t, t0, t1);
         l += t0 + t1;
       }
-      fence_async_smem();
       if (warp_rescale) {
         // O is stable once the P V of block j - 1 is done
         if (!mbar_wait(&pvdone[b ^ 1], ((j - 1) >> 1) & 1, abort_flag, &s_attn_status)) {
@@ -394,8 +389,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(tO + lane_off + hf * 64 + cc * 32, o);
         }
-        tmem_st_wait();
       }
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&pfull[b]);
     }
