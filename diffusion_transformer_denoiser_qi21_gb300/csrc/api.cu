@@ -544,16 +544,14 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
     const qi21_layer& w = layers[l];
     const bool last = (l + 1 == L);
     GemmPlan pq, po, p13, p2;
-    QI21_CK(make_gemm_plan(&pq, EPI_F16, M, 3 * H, H, b.xn, static_cast<const __half*>(w.wqkv),
+    // qkv projection with the qk RMSNorm + RoPE fused into its epilogue
+    QI21_CK(make_gemm_plan(&pq, EPI_QKV, M, 3 * H, H, b.xn, static_cast<const __half*>(w.wqkv),
                            b.panel, 3 * H, nullptr),
             "qkv plan");
+    pq.qkv = QkvEpi{w.norm_q, w.norm_k, g->eps, H, tabs};
     {
       ProfScope ps(QI21_CLASS_QKV, s);
       QI21_CK(launch_gemm(pq, s), "qkv gemm");
-    }
-    {
-      ProfScope ps(QI21_CLASS_QKROPE, s);
-      QI21_CK(launch_qkrope(M, g->heads, g->eps, b.panel, w.norm_q, w.norm_k, tabs, s), "qkrope");
     }
     AttnArgs aa{};
     aa.panel = b.panel;

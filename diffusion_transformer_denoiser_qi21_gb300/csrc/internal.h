@@ -43,7 +43,17 @@ cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half
 
 // ------------------------------------------------------------------ GEMM ----
 
-enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3 };
+enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4 };
+
+// Extra inputs of the EPI_QKV epilogue: per-head RMSNorm weights of q and k,
+// epsilon, the model width and the RoPE tables of the rows.
+struct QkvEpi {
+  const float* norm_q;
+  const float* norm_k;
+  float eps;
+  int H;
+  RopeTables tabs;
+};
 
 struct GemmPlan {
   CUtensorMap tmA;  // A f16 [M][K], box 64 x 128, 128B swizzle
@@ -51,6 +61,7 @@ struct GemmPlan {
   int M, N, K, bn, epi, ldo;
   void* out;
   const float* gate;
+  QkvEpi qkv;
 };
 
 // Encode the tensor maps of C = A B^T. Returns cudaSuccess or an error.

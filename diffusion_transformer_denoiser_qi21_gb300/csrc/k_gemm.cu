@@ -6,6 +6,10 @@
 //              projections followed by Qi21Dit::gated_add)
 //   EPI_SWIGLU silu(gate) * up on the interleaved gate/up plane
 //              (qwen_image21.rs, block_cpu: silu(gate) * proj)
+//   EPI_QKV    the qkv panel store with the per-head qk RMSNorm * w and the
+//              interleaved RoPE applied to the q and k columns on the way out
+//              (qwen_image21.rs, Qi21Dit::qk_norm_rope; each thread holds
+//              whole 128-column head vectors of its row)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
 // One persistent CTA per SM, 6 warps:
@@ -54,6 +58,7 @@ struct EpiArgs {
   void* out;
   int ldo;
   const float* gate;
+  QkvEpi qkv;
 };
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
@@ -87,6 +92,74 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
             }
             dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_QKV) {
+    const QkvEpi& qe = ep.qkv;
+    __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo;
+    // this row's RoPE table (the sequence whose rows contain it)
+    int si = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxSeq; ++i)
+      if (i < qe.tabs.nsrc && row >= qe.tabs.src[i].row0) si = i;
+    const size_t trow = static_cast<size_t>(live ? row - qe.tabs.src[si].row0 : 0) * 64;
+    const float4* cs4 = reinterpret_cast<const float4*>(qe.tabs.src[si].cos_ + trow);
+    const float4* sn4 = reinterpret_cast<const float4*>(qe.tabs.src[si].sin_ + trow);
+#pragma unroll 1
+    for (int hc = 0; hc < BN / 128; ++hc) {
+      const int col = n0 + hc * 128;
+      const int part = col / qe.H;  // 0 q, 1 k, 2 v (uniform over the tile)
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tbase + hc * 128 + c * 32, r[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
+      if (!live) continue;
+      uint4* dst = reinterpret_cast<uint4*>(out + col);
+      if (part == 2) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[c * 4 + j] = make_uint4(
+                pack_half2(__uint_as_float(r[c][8 * j + 0]), __uint_as_float(r[c][8 * j + 1])),
+                pack_half2(__uint_as_float(r[c][8 * j + 2]), __uint_as_float(r[c][8 * j + 3])),
+                pack_half2(__uint_as_float(r[c][8 * j + 4]), __uint_as_float(r[c][8 * j + 5])),
+                pack_half2(__uint_as_float(r[c][8 * j + 6]), __uint_as_float(r[c][8 * j + 7])));
+        continue;
+      }
+      float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float v = __uint_as_float(r[c][e]);
+          ss[e & 3] = fmaf(v, v, ss[e & 3]);
+        }
+      const float inv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / 128.f) + qe.eps);
+      const float4* w4 = reinterpret_cast<const float4*>(part == 0 ? qe.norm_q : qe.norm_k);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // elements 32c + 8j .. +7 = pairs 16c + 4j .. +3
+          const float4 wa = __ldg(w4 + 8 * c + 2 * j);
+          const float4 wb = __ldg(w4 + 8 * c + 2 * j + 1);
+          const float4 cv = __ldg(cs4 + 4 * c + j);
+          const float4 sv = __ldg(sn4 + 4 * c + j);
+          const float a0 = __uint_as_float(r[c][8 * j + 0]) * inv * wa.x;
+          const float b0 = __uint_as_float(r[c][8 * j + 1]) * inv * wa.y;
+          const float a1 = __uint_as_float(r[c][8 * j + 2]) * inv * wa.z;
+          const float b1 = __uint_as_float(r[c][8 * j + 3]) * inv * wa.w;
+          const float a2 = __uint_as_float(r[c][8 * j + 4]) * inv * wb.x;
+          const float b2 = __uint_as_float(r[c][8 * j + 5]) * inv * wb.y;
+          const float a3 = __uint_as_float(r[c][8 * j + 6]) * inv * wb.z;
+          const float b3 = __uint_as_float(r[c][8 * j + 7]) * inv * wb.w;
+          dst[c * 4 + j] = make_uint4(pack_half2(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
+                                      pack_half2(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
+                                      pack_half2(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
+                                      pack_half2(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
         }
       }
     }
@@ -302,6 +375,7 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   p->ldo = ldo;
   p->out = out;
   p->gate = gate;
+  p->qkv = QkvEpi{};
   p->bn = (N % 256 == 0) ? 256 : 128;
   cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
   if (e != cudaSuccess) return e;
@@ -320,7 +394,7 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   }
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / BN);
   const int grid = std::min(tiles, sm_count());
-  EpiArgs ep{p.out, p.ldo, p.gate};
+  EpiArgs ep{p.out, p.ldo, p.gate, p.qkv};
   gemm_tc_kernel<BN, EPI><<<grid, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.M, p.N, p.K, ep);
   return cudaGetLastError();
 }
@@ -333,6 +407,7 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
       case EPI_F32: return launch_t<256, EPI_F32>(p, s);
       case EPI_RESID: return launch_t<256, EPI_RESID>(p, s);
       case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU>(p, s);
+      case EPI_QKV: return launch_t<256, EPI_QKV>(p, s);
     }
   } else {
     switch (p.epi) {
@@ -340,6 +415,7 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
       case EPI_F32: return launch_t<128, EPI_F32>(p, s);
       case EPI_RESID: return launch_t<128, EPI_RESID>(p, s);
       case EPI_SWIGLU: return launch_t<128, EPI_SWIGLU>(p, s);
+      case EPI_QKV: return launch_t<128, EPI_QKV>(p, s);
     }
   }
   return cudaErrorInvalidValue;
