@@ -58,6 +58,7 @@ struct QkvEpi {
 struct GemmPlan {
   CUtensorMap tmA;  // A f16 [M][K], box 64 x 128, 128B swizzle
   CUtensorMap tmB;  // B f16 [N][K], box 64 x BN, 128B swizzle
+  CUtensorMap tmBh; // B f16 [N][K], box 64 x BN/2 (split tiles of a partial last wave)
   int M, N, K, bn, epi, ldo;
   void* out;
   const float* gate;

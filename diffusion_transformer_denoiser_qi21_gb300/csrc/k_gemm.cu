@@ -64,13 +64,13 @@ struct EpiArgs {
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
 
 template <int BN, int EPI>
-__device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0,
+__device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0, int bn,
                                               const EpiArgs& ep) {
   const bool live = row < M;
   if constexpr (EPI == EPI_SWIGLU) {
     __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
 #pragma unroll 1
-    for (int p = 0; p < BN / 128; ++p) {
+    for (int p = 0; p < bn / 128; ++p) {
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t g[32], u[32];
@@ -107,7 +107,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     const float4* cs4 = reinterpret_cast<const float4*>(qe.tabs.src[si].cos_ + trow);
     const float4* sn4 = reinterpret_cast<const float4*>(qe.tabs.src[si].sin_ + trow);
 #pragma unroll 1
-    for (int hc = 0; hc < BN / 128; ++hc) {
+    for (int hc = 0; hc < bn / 128; ++hc) {
       const int col = n0 + hc * 128;
       const int part = col / qe.H;  // 0 q, 1 k, 2 v (uniform over the tile)
       uint32_t r[4][32];
@@ -165,7 +165,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     }
   } else {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < bn / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tbase + c * 32, r);
       tmem_ld_wait(r);
@@ -207,10 +207,27 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
   }
 }
 
+// Tile t of the persistent schedule: the first nfull tiles are BM x BN;
+// when the last wave would be at most half full, its tiles are split into
+// two BM x BN/2 halves (same K order per output element, so identical
+// results) that fill one half-length wave instead.
+struct TileInfo {
+  int m0, n0, bn;
+};
+
+template <int BN>
+__device__ __forceinline__ TileInfo tile_at(int t, int num_m, int nfull) {
+  if (t < nfull) return TileInfo{(t % num_m) * kBM, (t / num_m) * BN, BN};
+  const int u = t - nfull;
+  const int tf = nfull + (u >> 1);
+  return TileInfo{(tf % num_m) * kBM, (tf / num_m) * BN + (u & 1) * (BN / 2), BN / 2};
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   int M, int N, int K, EpiArgs ep) {
+                   const __grid_constant__ CUtensorMap tmBh, int M, int N, int K, int nfull,
+                   int num_tiles, EpiArgs ep) {
   using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -225,7 +242,6 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_m = (M + kBM - 1) / kBM;
-  const int num_tiles = num_m * (N / BN);
   const int nk = K / kBK;
 
   if (threadIdx.x == 0) {
@@ -243,6 +259,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (nfull < num_tiles) tma_prefetch_desc(&tmBh);
   }
   if (warp == 1) {
     tmem_alloc(tslot, C::kTmemCols);
@@ -259,17 +276,18 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const int m0 = (t % num_m) * kBM;
-        const int n0 = (t / num_m) * BN;
+        const TileInfo ti = tile_at<BN>(t, num_m, nfull);
+        const bool half = ti.bn != BN;
+        const uint32_t bytes = C::kABytes + static_cast<uint32_t>(ti.bn) * kBK * 2;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, &s_gemm_status)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + s * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          tma_load_2d(sa, &tmA, &full[s], kb * kBK, m0);
-          tma_load_2d(sa + C::kABytes, &tmB, &full[s], kb * kBK, n0);
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * kBK, ti.m0);
+          tma_load_2d(sa + C::kABytes, half ? &tmBh : &tmB, &full[s], kb * kBK, ti.n0);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -279,12 +297,14 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kBM, BN);
+      constexpr uint32_t idesc_full = idesc_f16(kBM, BN);
+      constexpr uint32_t idesc_half = idesc_f16(kBM, BN / 2);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const uint32_t idesc = t < nfull ? idesc_full : idesc_half;
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, &s_gemm_status)) break;
@@ -315,14 +335,13 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const int m0 = (t % num_m) * kBM;
-      const int n0 = (t / num_m) * BN;
+      const TileInfo ti = tile_at<BN>(t, num_m, nfull);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      gemm_epilogue<BN, EPI>(tbase, m0 + q * 32 + lane, M, n0, ep);
+      gemm_epilogue<BN, EPI>(tbase, ti.m0 + q * 32 + lane, M, ti.n0, ti.bn, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
@@ -379,7 +398,9 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   p->bn = (N % 256 == 0) ? 256 : 128;
   cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
   if (e != cudaSuccess) return e;
-  return encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn);
+  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn);
+  if (e != cudaSuccess) return e;
+  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2);
 }
 
 template <int BN, int EPI>
@@ -393,9 +414,17 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     attr_done = true;
   }
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / BN);
-  const int grid = std::min(tiles, sm_count());
+  const int sms = sm_count();
+  // split the tiles of a partial last wave that is at most half full
+  int nfull = tiles, total = tiles;
+  const int rem = tiles % sms;
+  if (BN == 256 && tiles > sms && rem != 0 && 2 * rem <= sms) {
+    nfull = tiles - rem;
+    total = nfull + 2 * rem;
+  }
+  const int grid = std::min(total, sms);
   EpiArgs ep{p.out, p.ldo, p.gate, p.qkv};
-  gemm_tc_kernel<BN, EPI><<<grid, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.M, p.N, p.K, ep);
+  gemm_tc_kernel<BN, EPI><<<grid, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull, total, ep);
   return cudaGetLastError();
 }
 

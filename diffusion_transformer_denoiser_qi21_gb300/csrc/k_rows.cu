@@ -29,71 +29,75 @@ cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t
 }
 
 // ---------------------------------------------------------------- rowop ----
-// One 128-thread CTA per row, the row held in registers (dim <= 8192):
+// One 256-thread CTA per row, the row held in registers (NV float4 per
+// thread, NV = dim / 1024 rounded up to a power of two, dim <= 8192):
 //   if y:  x += gate_t * y            (qwen_image21.rs, Qi21Dit::gated_add)
 //   if xn: xn = f16(LN(x) (1 + scale)) (Qi21Dit::norm_mod; affine-free LN,
 //          biased variance, two passes over the registers in f32)
-constexpr int kRowThreads = 128;
-constexpr int kRowMaxVec = 16;  // float4 per thread -> dim <= 8192
+constexpr int kRowThreads = 256;
 
-__device__ __forceinline__ float block_sum_128(float v, float* red) {
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int w = threadIdx.x >> 5;
   __syncthreads();
   if ((threadIdx.x & 31) == 0) red[w] = v;
   __syncthreads();
-  return red[0] + red[1] + red[2] + red[3];
+  return ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
 }
 
+template <int NV>
 __global__ void __launch_bounds__(kRowThreads) rowop_kernel(int dim, float eps, float* __restrict__ x,
                                                             const float* __restrict__ y,
                                                             const float* __restrict__ gate_t,
                                                             const float* __restrict__ scale,
                                                             __half* __restrict__ xn) {
-  __shared__ float red[4];
+  __shared__ float red[8];
   const size_t row = blockIdx.x;
   const int nv = dim >> 2;
   float4* x4 = reinterpret_cast<float4*>(x + row * dim);
-  float4 v[kRowMaxVec];
+  float4 v[NV];
 #pragma unroll
-  for (int j = 0; j < kRowMaxVec; ++j) {
+  for (int j = 0; j < NV; ++j) {
     const int idx = threadIdx.x + j * kRowThreads;
-    if (idx < nv) {
-      float4 a = x4[idx];
-      if (y != nullptr) {
+    if (idx < nv) v[j] = x4[idx];
+  }
+  if (y != nullptr) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int idx = threadIdx.x + j * kRowThreads;
+      if (idx < nv) {
         const float4 b = reinterpret_cast<const float4*>(y + row * dim)[idx];
         const float4 g = reinterpret_cast<const float4*>(gate_t)[idx];
-        a.x = fmaf(g.x, b.x, a.x);
-        a.y = fmaf(g.y, b.y, a.y);
-        a.z = fmaf(g.z, b.z, a.z);
-        a.w = fmaf(g.w, b.w, a.w);
-        x4[idx] = a;
+        v[j].x = fmaf(g.x, b.x, v[j].x);
+        v[j].y = fmaf(g.y, b.y, v[j].y);
+        v[j].z = fmaf(g.z, b.z, v[j].z);
+        v[j].w = fmaf(g.w, b.w, v[j].w);
+        x4[idx] = v[j];
       }
-      v[j] = a;
     }
   }
   if (xn == nullptr) return;
   float sm = 0.f;
 #pragma unroll
-  for (int j = 0; j < kRowMaxVec; ++j)
+  for (int j = 0; j < NV; ++j)
     if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-  const float mean = block_sum_128(sm, red) / static_cast<float>(dim);
+  const float mean = block_sum_256(sm, red) / static_cast<float>(dim);
   float sq = 0.f;
 #pragma unroll
-  for (int j = 0; j < kRowMaxVec; ++j) {
+  for (int j = 0; j < NV; ++j) {
     if (threadIdx.x + j * kRowThreads < nv) {
       const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
       sq += (a * a + b * b) + (c * c + d * d);
     }
   }
-  const float inv = rsqrtf(block_sum_128(sq, red) / static_cast<float>(dim) + eps);
+  const float inv = rsqrtf(block_sum_256(sq, red) / static_cast<float>(dim) + eps);
   uint2* o2 = reinterpret_cast<uint2*>(xn + row * dim);
 #pragma unroll
-  for (int j = 0; j < kRowMaxVec; ++j) {
+  for (int j = 0; j < NV; ++j) {
     const int idx = threadIdx.x + j * kRowThreads;
     if (idx < nv) {
-      const float4 sc = reinterpret_cast<const float4*>(scale)[idx];
+      const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
       uint2 out;
       out.x = pack_half2((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
       out.y = pack_half2((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
@@ -105,7 +109,15 @@ __global__ void __launch_bounds__(kRowThreads) rowop_kernel(int dim, float eps, 
 cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
                          const float* scale, __half* xn, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  rowop_kernel<<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+  const int per = (dim / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
+  if (per <= 1)
+    rowop_kernel<1><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+  else if (per <= 2)
+    rowop_kernel<2><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+  else if (per <= 4)
+    rowop_kernel<4><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+  else
+    rowop_kernel<8><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
   return cudaGetLastError();
 }
 

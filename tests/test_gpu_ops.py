@@ -248,3 +248,33 @@ def test_attention_prefill_mask(segs):
     panel = S.op_tensor(9, lp, 0, (lp, 3 * H), 1.0).astype(np.float16)
     if vis[0] == 1:
         np.testing.assert_allclose(got[0], panel[0, 2 * H:].astype(np.float64), atol=2 * U16 * 4)
+
+
+@pytest.mark.parametrize("epi", ["resid", "swiglu"])
+def test_gemm_partial_last_wave_split(epi):
+    # 4096 x 4096 (512 tiles of 128 x 256) and 4096 x 24576 (3072 tiles): the
+    # tiles of the partial last wave run as 128 x 128 halves; sampled rows
+    # cover the last M tiles, where the split tiles sit
+    M, K = 4096, 512
+    rows = np.array([0, 127, 2048, 2175, 3968, 4000, 4095])
+    A = S.op_tensor(10, 1, 0, (M, K), 1.0).astype(np.float16)
+    a = A[rows].astype(np.float64)
+    if epi == "resid":
+        N = 4096
+        Bw = S.op_tensor(10, 1, 1, (N, K), K ** -0.5).astype(np.float16)
+        x0 = S.op_tensor(10, 1, 2, (M, N), 1.0)
+        gt = np.tanh(S.op_tensor(10, 1, 3, (N,), 0.1))
+        xd = T(x0)
+        q.op_gemm(q.EPI_RESID, T(A), T(Bw), xd, gate_t=T(gt))
+        got = xd[torch.from_numpy(rows).cuda()].cpu().numpy()
+        ref = x0[rows] + gt.astype(np.float64) * (a @ Bw.astype(np.float64).T)
+        assert np.max(np.abs(got - ref)) < 1e-4
+    else:
+        I = 12288
+        G = S.op_tensor(10, 2, 1, (I, K), K ** -0.5).astype(np.float16)
+        Up = S.op_tensor(10, 2, 2, (I, K), K ** -0.5).astype(np.float16)
+        out = torch.empty((M, I), dtype=torch.float16, device="cuda")
+        q.op_gemm(q.EPI_SWIGLU, T(A), T(_interleave_w13(G, Up)), out)
+        got = out[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+        ref = O.silu(a @ G.astype(np.float64).T) * (a @ Up.astype(np.float64).T)
+        assert np.all(np.abs(got - ref) <= 2 * U16 * np.abs(ref) + 2e-3)
