@@ -12,11 +12,16 @@
 //              whole 128-column head vectors of its row)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
-// One persistent CTA per SM, 6 warps:
-//   warp 0     TMA producer: A 128x64 and B BNx64 tiles (128-byte swizzle)
-//              into a STAGES-deep shared-memory ring (full/empty mbarriers)
+// Persistent clusters of two CTAs (one per SM). The two CTAs of a cluster
+// compute vertically adjacent 128 x BN tiles with the same weight columns:
+// each loads its own A rows and HALF of the shared B tile, multicast into
+// both CTAs' shared memory, so each SM reads a third less from L2. 6 warps:
+//   warp 0     TMA producer: A 128x64 (own) and B (BN/2)x64 (multicast) tiles
+//              (128-byte swizzle) into a STAGES-deep shared-memory ring; a
+//              stage is refilled only once BOTH CTAs' MMAs have released it
 //   warp 1     TMEM allocator and single-thread MMA issuer
-//              (tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16)
+//              (tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16); its
+//              commits release the stage in both CTAs (multicast arrive)
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane quadrant, fused op,
 //              128-bit stores; two TMEM accumulators so the epilogue of tile
 //              i overlaps the MMAs of tile i+1.
@@ -207,24 +212,25 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
   }
 }
 
-// Tile t of the persistent schedule: the first nfull tiles are BM x BN;
-// when the last wave would be at most half full, its tiles are split into
-// two BM x BN/2 halves (same K order per output element, so identical
-// results) that fill one half-length wave instead.
+// Tile pair t of the persistent schedule (one pair per cluster step): the
+// first nfull pairs are 2 x (BM x BN) with pair row mp (tile rows 2 mp and
+// 2 mp + 1) and column block n; when the last wave would be at most half
+// full, its pairs are split into two halves of BN/2 columns (same K order
+// per output element, so identical results) that fill one half-length wave.
 struct TileInfo {
-  int m0, n0, bn;
+  int mp, n0, bn;
 };
 
 template <int BN>
-__device__ __forceinline__ TileInfo tile_at(int t, int num_m, int nfull) {
-  if (t < nfull) return TileInfo{(t % num_m) * kBM, (t / num_m) * BN, BN};
+__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nfull) {
+  if (t < nfull) return TileInfo{t % num_mp, (t / num_mp) * BN, BN};
   const int u = t - nfull;
   const int tf = nfull + (u >> 1);
-  return TileInfo{(tf % num_m) * kBM, (tf / num_m) * BN + (u & 1) * (BN / 2), BN / 2};
+  return TileInfo{tf % num_mp, (tf / num_mp) * BN + (u & 1) * (BN / 2), BN / 2};
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, int M, int N, int K, int nfull,
                    int num_tiles, EpiArgs ep) {
@@ -241,13 +247,16 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_m = (M + kBM - 1) / kBM;
+  const int rank = static_cast<int>(cluster_rank());
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int num_mp = ((M + kBM - 1) / kBM + 1) / 2;
   const int nk = K / kBK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 2);  // both CTAs' MMAs release a stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
@@ -275,9 +284,12 @@ __global__ void __launch_bounds__(192, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = tile_at<BN>(t, num_m, nfull);
+      for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+        const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
         const bool half = ti.bn != BN;
+        const int m0 = (2 * ti.mp + rank) * kBM;
+        const int bh = ti.bn / 2;  // B rows this CTA loads for both
+        // own A + own half of B + the partner's half of B
         const uint32_t bytes = C::kABytes + static_cast<uint32_t>(ti.bn) * kBK * 2;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, &s_gemm_status)) {
@@ -286,8 +298,9 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sa = smem + s * C::kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(sa, &tmA, &full[s], kb * kBK, ti.m0);
-          tma_load_2d(sa + C::kABytes, half ? &tmBh : &tmB, &full[s], kb * kBK, ti.n0);
+          tma_load_2d(sa, &tmA, &full[s], kb * kBK, m0);
+          tma_load_2d_mc(sa + C::kABytes + rank * bh * kBK * 2, half ? &tmBh : &tmB, &full[s], kb * kBK,
+                         ti.n0 + rank * bh, 0x3);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -303,7 +316,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
         const uint32_t idesc = t < nfull ? idesc_full : idesc_half;
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             tc_mma_f16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          tc_commit(&empty[s]);
+          tc_commit_mc(&empty[s], 0x3);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -334,22 +347,23 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int it = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const TileInfo ti = tile_at<BN>(t, num_m, nfull);
+    for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
+      const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      gemm_epilogue<BN, EPI>(tbase, ti.m0 + q * 32 + lane, M, ti.n0, ti.bn, ep);
+      gemm_epilogue<BN, EPI>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
   }
+  // the partner may still be signalling this CTA's barriers: leave together
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -398,33 +412,43 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   p->bn = (N % 256 == 0) ? 256 : 128;
   cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
   if (e != cudaSuccess) return e;
-  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn);
+  // each CTA of a cluster loads half of the B tile (and a quarter in the
+  // split tail)
+  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2);
   if (e != cudaSuccess) return e;
-  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2);
+  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4);
 }
 
 template <int BN, int EPI>
 static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   using C = GemmCfg<BN>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sm_count(), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI>, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
   }
-  const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / BN);
-  const int sms = sm_count();
-  // split the tiles of a partial last wave that is at most half full
-  int nfull = tiles, total = tiles;
-  const int rem = tiles % sms;
-  if (BN == 256 && tiles > sms && rem != 0 && 2 * rem <= sms) {
-    nfull = tiles - rem;
+  const int num_mp = ((p.M + kBM - 1) / kBM + 1) / 2;
+  const int pairs = num_mp * (p.N / BN);
+  // split the pairs of a partial last wave that is at most half full
+  int nfull = pairs, total = pairs;
+  const int rem = pairs % max_clusters;
+  if (BN == 256 && pairs > max_clusters && rem != 0 && 2 * rem <= max_clusters) {
+    nfull = pairs - rem;
     total = nfull + 2 * rem;
   }
-  const int grid = std::min(total, sms);
+  const int clusters = std::min(total, max_clusters);
   EpiArgs ep{p.out, p.ldo, p.gate, p.qkv};
-  gemm_tc_kernel<BN, EPI><<<grid, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull, total, ep);
+  gemm_tc_kernel<BN, EPI><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull,
+                                                               total, ep);
   return cudaGetLastError();
 }
 
