@@ -12,19 +12,23 @@
 //              whole 128-column head vectors of its row)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
-// Persistent clusters of two CTAs (one per SM). The two CTAs of a cluster
-// compute vertically adjacent 128 x BN tiles with the same weight columns:
-// each loads its own A rows and HALF of the shared B tile, multicast into
-// both CTAs' shared memory, so each SM reads a third less from L2. 6 warps:
-//   warp 0     TMA producer: A 128x64 (own) and B (BN/2)x64 (multicast) tiles
-//              (128-byte swizzle) into a STAGES-deep shared-memory ring; a
-//              stage is refilled only once BOTH CTAs' MMAs have released it
-//   warp 1     TMEM allocator and single-thread MMA issuer
-//              (tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16); its
-//              commits release the stage in both CTAs (multicast arrive)
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quadrant, fused op,
-//              128-bit stores; two TMEM accumulators so the epilogue of tile
-//              i overlaps the MMAs of tile i+1.
+// Persistent clusters of two CTAs (one per SM) running the pair MMA
+// (tcgen05.mma.cta_group::2, a 256 x BN tile per CTA pair): CTA r holds rows
+// [128 r, 128 r + 128) of the A tile and rows [BN/2 r, BN/2 r + BN/2) of
+// the B tile in its shared memory, and receives rows [128 r, 128 r + 128)
+// of the accumulator in its TMEM. Each SM therefore holds only half of B:
+// 32 KB stages instead of 48 KB, six of them, enough operand data in flight
+// to cover the TMA latency. 6 warps per CTA:
+//   warp 0     TMA producer (both CTAs): A 128x64 and B (BN/2)x64 tiles
+//              (128-byte swizzle) into a 6-stage ring; the loads of both CTAs
+//              complete on the even CTA's "full" mbarrier
+//   warp 1     TMEM allocation (jointly, both CTAs); in the even CTA one
+//              thread issues the pair MMAs (M=256, N=BN, K=16) and commits
+//              that release a stage / publish an accumulator in both CTAs
+//   warps 2-5  epilogue (both CTAs): tcgen05.ld of their 32-lane quadrant,
+//              fused op, 128-bit stores; two TMEM accumulators so the
+//              epilogue of tile i overlaps the MMAs of tile i+1; each warp
+//              reports "accumulator free" to the even CTA.
 #include <algorithm>
 #include <cstdio>
 
@@ -50,10 +54,10 @@ constexpr int kBK = 64;
 
 template <int BN>
 struct GemmCfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kABytes = kBM * kBK * 2;        // this CTA's A rows
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;   // this CTA's half of B
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
@@ -248,6 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_rank());
+  const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
   const int num_mp = ((M + kBM - 1) / kBM + 1) / 2;
@@ -255,12 +260,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 2);  // both CTAs' MMAs release a stage
+      mbar_init(&full[i], 1);   // the even CTA's producer (+ both CTAs' bytes)
+      mbar_init(&empty[i], 1);  // the pair-MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 8);  // 4 epilogue warps x 2 CTAs
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -271,11 +276,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (nfull < num_tiles) tma_prefetch_desc(&tmBh);
   }
   if (warp == 1) {
-    tmem_alloc(tslot, C::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tslot, C::kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised before any multicast
+  cluster_sync();  // both CTAs' barriers and TMEM ready before any remote use
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
@@ -288,19 +293,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
         const bool half = ti.bn != BN;
         const int m0 = (2 * ti.mp + rank) * kBM;
-        const int bh = ti.bn / 2;  // B rows this CTA loads for both
-        // own A + own half of B + the partner's half of B
-        const uint32_t bytes = C::kABytes + static_cast<uint32_t>(ti.bn) * kBK * 2;
+        const int bh = ti.bn / 2;  // B rows this CTA holds
+        // the even CTA's barrier counts both CTAs' A and B bytes
+        const uint32_t bytes = 2u * (C::kABytes + static_cast<uint32_t>(bh) * kBK * 2);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, &s_gemm_status)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + s * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(sa, &tmA, &full[s], kb * kBK, m0);
-          tma_load_2d_mc(sa + C::kABytes + rank * bh * kBK * 2, half ? &tmBh : &tmB, &full[s], kb * kBK,
-                         ti.n0 + rank * bh, 0x3);
+          const uint32_t fb = mapa_rank(&full[s], 0);
+          if (leader) mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
+          tma_load_2d_pair(sa + C::kABytes, half ? &tmBh : &tmB, fb, kb * kBK, ti.n0 + rank * bh);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -309,9 +314,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_full = idesc_f16(kBM, BN);
-      constexpr uint32_t idesc_half = idesc_f16(kBM, BN / 2);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc_full = idesc_f16(2 * kBM, BN);
+      constexpr uint32_t idesc_half = idesc_f16(2 * kBM, BN / 2);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
@@ -334,14 +339,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            tc_mma_f16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          tc_commit_mc(&empty[s], 0x3);
+            tc_mma_f16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair(&empty[s], 0x3);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (ok) tc_commit(&tfull[acc]);
+        if (ok) tc_commit_pair(&tfull[acc], 0x3);
       }
     }
   } else {
@@ -356,7 +361,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
       gemm_epilogue<BN, EPI>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_rank(&tempty[acc], 0));
     }
   }
   // the partner may still be signalling this CTA's barriers: leave together
@@ -365,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc_pair(tmem, C::kTmemCols);
   }
 }
 
