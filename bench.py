@@ -75,6 +75,36 @@ def class_work(w, n_rows, vis_sum):
     }
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
+# of two launches) from one single-pass ncu capture of this benchmark's
+# default workload, with the sha256 of the kernel's source at capture time
+# (profiles/dram_traffic_step32_cond4114_n4096.md). Reported only while the
+# source is unchanged.
+NCU_TRAFFIC = {
+    "attention": ("k_attn.cu", "31e2c2f8ce3fc70b353bdbeae0edc7a3ab41c6cf149584d9d5ab604720533dd2",
+                  168198400 + 20426880),
+    "gateup": ("k_gemm.cu", "7a532772def56fdd53aebf3366366c284d84f1360d65f94d35884df375714ad2",
+               249069568 + 87047808),
+}
+
+
+def measured_traffic(kernel_class, workload):
+    """ncu DRAM bytes per launch of a kernel class, or None if there is no
+    capture for this workload or the kernel's source changed since."""
+    import hashlib
+    if workload != DEFAULT_WORKLOAD or kernel_class not in NCU_TRAFFIC:
+        return None
+    fname, sha, nbytes = NCU_TRAFFIC[kernel_class]
+    path = os.path.join(ROOT, "diffusion_transformer_denoiser_qi21_gb300", "csrc", fname)
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    return float(nbytes)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -399,7 +429,8 @@ def run_gpu(args):
     roofline = {
         "kernel": dom, "bound": "tensor" if kind == "flop" else "hbm", "achieved": dk["achieved"],
         "peak": peaks["bf16_tflops_sustained"] if kind == "flop" else peaks["hbm_gbs"],
-        "unit": dk["unit"], "frac": dk["frac"], "traffic": None,
+        "unit": dk["unit"], "frac": dk["frac"], "traffic": measured_traffic(dom, w.name),
+        "traffic_unit": "bytes per launch",
         "peak_source": f"{peak_src}: " + ("bf16_tflops_sustained (f16 dense rate = bf16 dense rate)"
                                           if kind == "flop" else "hbm_gbs"),
         "algorithmic_per_launch": amount,
