@@ -354,6 +354,29 @@ def joint_forward(x_prefix, x_target, weights, mods0, mods, segs, cfg):
     return x[lp:]
 
 
+def embed_image(tok, w_in):
+    """img_in: latent tokens [n, in_channels] -> hidden states [n, dim],
+    no bias (qwen_image21.rs, Qi21Dit::embed_image): x = tok W_in^T with
+    W_in [dim, in_channels]."""
+    return np.asarray(tok, dtype=np.float64) @ np.asarray(w_in, dtype=np.float64).T
+
+
+def final_layer(x, final_scale, w_out, eps):
+    """After the blocks: LN(x)(1 + final_scale), then proj_out [out, dim]
+    with no bias (qwen_image21.rs, Qi21Dit::step_cpu, the last two
+    statements; the device path passes fs = 1 + final_scale)."""
+    return norm_mod(x, final_scale, eps) @ np.asarray(w_out, dtype=np.float64).T
+
+
+def denoise(tok, w_in, weights, mods, final_scale, w_out, segs, cache, cfg):
+    """One denoiser call: latent tokens -> velocity (qwen_image21.rs,
+    Qi21Dit::step_cpu): embed_image, the blocks against the cached prefix,
+    the final modulated LayerNorm and proj_out."""
+    x = embed_image(tok, w_in)
+    x, _ = step(x, weights, mods, segs, cache, cfg)
+    return final_layer(x, final_scale, w_out, cfg["eps"])
+
+
 def mods_dev(mods, h):
     """[s1 | tanh g1 | s2 | tanh g2]: the gate chunks tanh-ed in f32, the
     scale chunks as they are (qi21.rs, mods_dev)."""

@@ -18,7 +18,10 @@ Recipe (one stream per tensor, so any single tensor can be rebuilt alone):
 * projection weights ~ N(0, fan_in^-1/2) (standard deviation), rounded to
   float16 (round to nearest even) -- the oracle widens exactly these values;
   fan_in = dim for q, k, v, o, gate, up and mlp_hidden for down;
-* per-head RMSNorm weights ``norm_q``, ``norm_k`` = 1 + N(0, 0.05) float32.
+* per-head RMSNorm weights ``norm_q``, ``norm_k`` = 1 + N(0, 0.05) float32;
+* latent tokens ~ N(0, 1) float32 [n, 64]; img_in weight ~ N(0, 64^-1/2)
+  and proj_out weight ~ N(0, dim^-1/2), float32 (the page keeps f32 copies
+  of both for its device path); final_scale ~ N(0, 0.1) float32.
 """
 from __future__ import annotations
 
@@ -44,6 +47,10 @@ TAG_ID = {
     "wdown": 16,
     "norm_q": 17,
     "norm_k": 18,
+    "tok": 30,          # latent tokens of the target image block
+    "w_in": 31,         # img_in
+    "w_out": 32,        # proj_out
+    "final_scale": 33,  # final modulation of norm_out
     "op_test": 50,  # single-operation checks: index = a case number
 }
 
@@ -183,6 +190,29 @@ def x_target(w: Workload) -> np.ndarray:
 def mods_t(w: Workload) -> np.ndarray:
     """Step modulation [scale1|gate1|scale2|gate2]: float32 [4·dim], N(0, 0.1)."""
     return normal(w.seed, "mods_t", 0, 4 * w.dim, 0.1)
+
+
+LATENT_CHANNELS = 64
+
+
+def tokens(w: Workload) -> np.ndarray:
+    """Latent tokens of the target image: float32 [n, 64], N(0, 1)."""
+    return normal(w.seed, "tok", 0, w.n_target * LATENT_CHANNELS, 1.0).reshape(w.n_target, LATENT_CHANNELS)
+
+
+def w_in(w: Workload) -> np.ndarray:
+    """img_in weight: float32 [dim, 64], N(0, 64^-1/2)."""
+    return normal(w.seed, "w_in", 0, w.dim * LATENT_CHANNELS, LATENT_CHANNELS ** -0.5).reshape(w.dim, LATENT_CHANNELS)
+
+
+def w_out(w: Workload) -> np.ndarray:
+    """proj_out weight: float32 [64, dim], N(0, dim^-1/2)."""
+    return normal(w.seed, "w_out", 0, LATENT_CHANNELS * w.dim, w.dim ** -0.5).reshape(LATENT_CHANNELS, w.dim)
+
+
+def final_scale(w: Workload) -> np.ndarray:
+    """Final modulation (norm_out scale) of the step: float32 [dim], N(0, 0.1)."""
+    return normal(w.seed, "final_scale", 0, w.dim, 0.1)
 
 
 def mods0(w: Workload) -> np.ndarray:

@@ -415,3 +415,49 @@ def test_flop_accounting_reproduces_measured_classes():
     gemm, attn = O.step_flops(H, I, L, n, n * (lp + n))
     assert gemm == sum(flops[k] for k in ("qkv", "o", "gateup", "down"))
     assert attn == flops["flash"]
+
+
+# ------------------------------------------------------ embed / final pins --
+
+def test_embed_image_closed_form():
+    # nn.Linear layout: x[r][c] = sum_k tok[r][k] W[c][k]
+    tok = np.array([[1.0, 2.0, 0.0], [0.0, -1.0, 3.0]])
+    W = np.array([[1.0, 0.0, 0.0], [0.0, 1.0, 0.0], [1.0, 1.0, 1.0], [2.0, 0.0, -1.0]])
+    want = np.array([[1.0, 2.0, 3.0, 2.0], [0.0, -1.0, 2.0, -3.0]])
+    np.testing.assert_array_equal(O.embed_image(tok, W), want)
+
+
+def test_final_layer_closed_form_and_constant_rows():
+    eps = 1e-6
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    fs = np.array([0.5, -1.0, 0.0, 1.0])
+    W = np.array([[1.0, 1.0, 1.0, 1.0], [0.0, 0.0, 0.0, 2.0]])
+    ln = (x[0] - 2.5) / math.sqrt(1.25 + eps)
+    xn = ln * (1.0 + fs)
+    want = [[xn.sum(), 2.0 * xn[3]]]
+    np.testing.assert_allclose(O.final_layer(x, fs, W, eps), want, atol=1e-14)
+    # a constant row normalises to zero whatever the scale and weight
+    c = np.full((2, 8), 3.25)
+    rng = np.random.default_rng(12)
+    assert np.all(O.final_layer(c, rng.standard_normal(8), rng.standard_normal((5, 8)), eps) == 0.0)
+
+
+def test_denoise_composes_embed_step_final():
+    rng = np.random.default_rng(13)
+    cfg = _tiny_cfg(dim=16, heads=2, head_dim=8, axes=(2, 2, 4))
+    H, I, C = 16, 24, 5
+    layers = [_rand_layer(rng, H, I, 8) for _ in range(2)]
+    segs = [(0, 3, 0), (1, 2, 3)]
+    lp, n = O.prefix_len(segs), O.seg_len(segs[-1])
+    tok = rng.standard_normal((n, C))
+    w_in = rng.standard_normal((H, C))
+    w_out = rng.standard_normal((C, H))
+    fsc = rng.standard_normal(H) * 0.1
+    m0, mt = rng.standard_normal(4 * H) * 0.2, rng.standard_normal(4 * H) * 0.2
+    cache, _ = O.prefill(rng.standard_normal((lp, H)), layers, m0, segs, cfg)
+    got = O.denoise(tok, w_in, layers, mt, fsc, w_out, segs, cache, cfg)
+    x = tok @ w_in.T
+    for l, W in enumerate(layers):
+        x, _, _ = O.block(x, W, mt, *O.target_rope(segs, cfg["axes"], cfg["theta"]), cfg, cache[l], None)
+    want = O.layer_norm(x, cfg["eps"]) * (1 + fsc) @ w_out.T
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
