@@ -72,6 +72,9 @@ def class_work(w, n_rows, vis_sum):
         "qkrope": ("byte", float(M) * (2 * H * 2 * 2 + 2 * 64 * 4)),
         "kvcopy": ("byte", float(M) * 2 * H * 2 * 2),
         "misc": ("byte", 4.0 * H * 4 * 2),
+        # tokens f32 read + x f32 written / x f32 read + velocity written
+        "embed": ("byte", float(M) * (64 + H) * 4),
+        "final": ("byte", float(M) * (H + 64) * 4),
     }
 
 
@@ -444,6 +447,36 @@ def run_gpu(args):
     fractions["gemm_frac"] = (fractions["gemm_tflops"] or 0) / peaks["bf16_tflops_sustained"]
     fractions["attention_frac"] = (fractions["attention_tflops"] or 0) / peaks["bf16_tflops_sustained"]
 
+    # the whole denoiser call of the pages (tokens -> embed -> blocks ->
+    # final -> velocity), timed on its own beside the step metric
+    denoise = None
+    if not args.no_e2e:
+        tok = torch.from_numpy(S.tokens(w)).cuda()
+        if w.nseq > 1:
+            tok = tok.repeat(w.nseq, 1).contiguous()
+        w_in = torch.from_numpy(S.w_in(w)).cuda()
+        w_out = torch.from_numpy(S.w_out(w)).cuda()
+        fsc = torch.from_numpy(S.final_scale(w)).cuda()
+        vel = torch.empty((n_rows, 64), device="cuda")
+        for _ in range(2):
+            q.denoise_batch(dw.g, dw.layers, dw.caches, tok, w_in, dw.mods_t, fsc, w_out, vel, dw.ws)
+        q.profile_enable(True)
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        nd = max(2, args.steps // 2)
+        for _ in range(nd):
+            q.denoise_batch(dw.g, dw.layers, dw.caches, tok, w_in, dw.mods_t, fsc, w_out, vel, dw.ws)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dms, _ = q.profile_read()
+        q.profile_enable(False)
+        ms = d0.elapsed_time(d1) / nd
+        denoise = {"ms": ms, "rows_per_s": n_rows / (ms * 1e-3), "calls": nd,
+                   "embed_ms": dms["embed"] / nd, "final_ms": dms["final"] / nd}
+        if q.device_status() != 0:
+            raise RuntimeError("a kernel gave up waiting during the denoiser calls")
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rps, spent, desc = oracle_layer_sample(w, args.cpu_rows)
@@ -459,6 +492,7 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
             "clocks": clk, "classes": classes, "fractions": fractions,
             "prefill": {"ms": prefill_ms, "rows": lp, "rows_per_s": sum(lp) / (prefill_ms * 1e-3)},
+            "denoise": denoise,
             "setup_s": t_setup,
         }
         print(json.dumps(line), flush=True)

@@ -17,7 +17,8 @@ from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_T
 
 __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
-    "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "device_status", "build",
+    "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
+    "denoise", "denoise_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -164,6 +165,40 @@ def step_noalloc(g: Geom, layers, cache: KVCache, x_in, x_out, mods, stream=None
     f = torch.float32
     check(load().qi21_step_noalloc(C.byref(g), _layer_array(layers), cache.handle, _ptr(x_in, f, "x_in"),
                                    _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _stream(stream)))
+
+
+def embed(tok, w_in, x, stream=None):
+    """qi21_embed: x [n, dim] = tok [n, 64] w_in^T (f32)."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_embed(tok.shape[0], x.shape[1], tok.shape[1], _ptr(tok, f, "tok"), _ptr(w_in, f, "w_in"),
+                            _ptr(x, f, "x"), _stream(stream)))
+
+
+def final(x, final_scale, w_out, out, eps=1e-6, stream=None):
+    """qi21_final: out [n, 64] = (LN(x)(1 + final_scale)) w_out^T (f32)."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_final(x.shape[0], x.shape[1], w_out.shape[0], eps, _ptr(x, f, "x"),
+                            _ptr(final_scale, f, "final_scale"), _ptr(w_out, f, "w_out"), _ptr(out, f, "out"),
+                            _stream(stream)))
+
+
+def denoise_batch(g: Geom, layers, caches, tok, w_in, mods, final_scale, w_out, out, workspace, stream=None):
+    """qi21_denoise_batch: latent tokens -> velocity for one or more sequences."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    check(load().qi21_denoise_batch(C.byref(g), _layer_array(layers), arr, len(caches), _ptr(tok, f, "tok"),
+                                    _ptr(w_in, f, "w_in"), _ptr(mods, f, "mods"),
+                                    _ptr(final_scale, f, "final_scale"), _ptr(w_out, f, "w_out"),
+                                    _ptr(out, f, "out"), _ptr(workspace, None, "workspace"),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def denoise(g: Geom, layers, cache, tok, w_in, mods, final_scale, w_out, out, workspace, stream=None):
+    """qi21_denoise: latent tokens [n, 64] -> velocity [n, 64]."""
+    denoise_batch(g, layers, [cache], tok, w_in, mods, final_scale, w_out, out, workspace, stream)
 
 
 def step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace, x_layers=None, stream=None):

@@ -72,6 +72,12 @@ _SIGS = {
     "qi21_step": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "qi21_step_batch": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), C.POINTER(_vp), _i32, _vp, _vp, _vp,
                                   _vp, _vp, _sz, _vp]),
+    "qi21_embed": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "qi21_final": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
+    "qi21_denoise_batch": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), C.POINTER(_vp), _i32, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, _sz, _vp]),
+    "qi21_denoise": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                               _vp]),
     "qi21_step_noalloc": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp]),
     "qi21_device_status": (C.c_int, []),
     "qi21_profile_enable": (C.c_int, [C.c_int]),
@@ -162,7 +168,7 @@ def device_status() -> int:
     return load().qi21_device_status()
 
 
-CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc")
+CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc", "embed", "final")
 
 
 def profile_enable(on: bool) -> None:

@@ -691,6 +691,73 @@ int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
   return run_pass(g, layers, M, false, nullptr, caches, nseq, n, b, x_layers, s);
 }
 
+int qi21_embed(int32_t n, int32_t dim, int32_t in_ch, const float* tok, const float* w_in, float* x,
+               void* stream) {
+  if (n < 0 || dim <= 0 || dim % 4) return fail(QI21_ERR_SHAPE, "n %d dim %d", n, dim);
+  if (in_ch != QI21_LATENT_CHANNELS) return fail(QI21_ERR_GEOM, "in_ch %d (the kernels take 64)", in_ch);
+  if (n == 0) return QI21_OK;
+  if (!tok || !w_in || !x) return fail(QI21_ERR_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(w_in) | reinterpret_cast<uintptr_t>(x)) % 16)
+    return fail(QI21_ERR_ARG, "w_in and x must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(QI21_CLASS_EMBED, s);
+  QI21_CK(launch_embed(n, dim, tok, w_in, x, s), "embed");
+  return QI21_OK;
+}
+
+int qi21_final(int32_t n, int32_t dim, int32_t out_ch, float eps, const float* x, const float* final_scale,
+               const float* w_out, float* out, void* stream) {
+  if (n < 0 || dim <= 0 || dim % 64) return fail(QI21_ERR_SHAPE, "n %d dim %d", n, dim);
+  if (out_ch != QI21_LATENT_CHANNELS) return fail(QI21_ERR_GEOM, "out_ch %d (the kernels take 64)", out_ch);
+  if (!(eps > 0.f)) return fail(QI21_ERR_ARG, "eps must be > 0");
+  if (n == 0) return QI21_OK;
+  if (!x || !final_scale || !w_out || !out) return fail(QI21_ERR_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(QI21_ERR_ARG, "x and out must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(QI21_CLASS_FINAL, s);
+  QI21_CK(launch_final(n, dim, eps, x, final_scale, w_out, out, s), "final");
+  return QI21_OK;
+}
+
+int qi21_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
+                       int32_t nseq, const float* tok, const float* w_in, const float* mods,
+                       const float* final_scale, const float* w_out, float* out, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (caches == nullptr || nseq < 1 || nseq > kMaxSeq) return fail(QI21_ERR_ARG, "caches / nseq");
+  if (!tok || !w_in || !mods || !final_scale || !w_out || !out) return fail(QI21_ERR_ARG, "null pointer");
+  for (int q = 0; q < nseq; ++q)
+    if (caches[q] == nullptr) return fail(QI21_ERR_ARG, "null cache %d", q);
+  const int n = caches[0]->n;
+  const int M = nseq * n;
+  PassBufs b;
+  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
+  // the full validation of the step runs before anything is enqueued
+  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
+  for (int q = 0; q < nseq; ++q) {
+    const qi21_kvcache* c = caches[q];
+    if (!same_geom(*g, c->g)) return fail(QI21_ERR_SHAPE, "cache %d was made for another geometry", q);
+    if (!c->filled) return fail(QI21_ERR_STATE, "cache %d has not been prefilled", q);
+    if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
+  }
+  if ((rc = qi21_embed(M, g->dim, QI21_LATENT_CHANNELS, tok, w_in, b.x, stream)) != QI21_OK) return rc;
+  if ((rc = qi21_step_batch(g, layers, caches, nseq, b.x, b.x, mods, nullptr, workspace, ws_bytes, stream)) !=
+      QI21_OK)
+    return rc;
+  return qi21_final(M, g->dim, QI21_LATENT_CHANNELS, g->eps, b.x, final_scale, w_out, out, stream);
+}
+
+int qi21_denoise(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache, const float* tok,
+                 const float* w_in, const float* mods, const float* final_scale, const float* w_out, float* out,
+                 void* workspace, size_t ws_bytes, void* stream) {
+  if (cache == nullptr) return fail(QI21_ERR_ARG, "null cache");
+  const qi21_kvcache* cs[1] = {cache};
+  return qi21_denoise_batch(g, layers, cs, 1, tok, w_in, mods, final_scale, w_out, out, workspace, ws_bytes,
+                            stream);
+}
+
 int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache,
               const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
               size_t ws_bytes, void* stream) {

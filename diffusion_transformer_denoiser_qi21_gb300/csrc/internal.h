@@ -41,6 +41,12 @@ cudaError_t launch_kvcopy(int rows, int dim, const __half* panel, __half* kv, cu
 cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half* up, __half* dst,
                             cudaStream_t s);
 
+// x[n][dim] = tok[n][64] w_in[dim][64]^T (f32)
+cudaError_t launch_embed(int n, int dim, const float* tok, const float* w_in, float* x, cudaStream_t s);
+// out[n][64] = (LN(x)(1 + fs)) w_out[64][dim]^T (f32)
+cudaError_t launch_final(int n, int dim, float eps, const float* x, const float* fs, const float* w_out,
+                         float* out, cudaStream_t s);
+
 // ------------------------------------------------------------------ GEMM ----
 
 enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4 };

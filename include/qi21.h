@@ -196,6 +196,44 @@ int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* 
               const float* x_in, float* x_out, const float* mods, float* x_layers,
               void* workspace, size_t ws_bytes, void* stream);
 
+/* Latent channels of the image tokens (qwen_image21.rs, Qi21Config::
+ * in_channels / out_channels; the page's device path requires 64). */
+#define QI21_LATENT_CHANNELS 64
+
+/* Image embedding (qwen_image21.rs, Qi21Dit::embed_image; gpu_wgpu/qi21.rs,
+ * zi_embed): x[n][dim] = tok[n][64] * w_in^T, no bias. tok device f32
+ * [n][64], w_in device f32 [dim][64] (img_in.weight), x device f32 [n][dim].
+ * in_ch must be 64; dim % 4 == 0. */
+int qi21_embed(int32_t n, int32_t dim, int32_t in_ch, const float* tok, const float* w_in, float* x,
+               void* stream);
+
+/* Final layer (qwen_image21.rs, Qi21Dit::step_cpu after the blocks;
+ * gpu_wgpu/qi21.rs, zi_final): out[n][64] = (LN(x) * (1 + final_scale)) *
+ * w_out^T, affine-free LN with biased variance, no bias. x device f32
+ * [n][dim], final_scale device f32 [dim] (raw, the norm_out scale of the
+ * step), w_out device f32 [64][dim] (proj_out.weight), out device f32
+ * [n][64]. out_ch must be 64; dim % 64 == 0. */
+int qi21_final(int32_t n, int32_t dim, int32_t out_ch, float eps, const float* x,
+               const float* final_scale, const float* w_out, float* out, void* stream);
+
+/* One whole denoiser call of `nseq` (1..8) sequences sharing the target
+ * size (qwen_image21.rs, Qi21Dit::step / step_cpu; gpu_wgpu/qi21.rs, step):
+ * latent tokens tok (device f32 [nseq*n][64]) -> embed -> the blocks against
+ * each sequence's cache (as qi21_step_batch) -> final layer -> velocity out
+ * (device f32 [nseq*n][64]). mods device f32 [4H] raw; final_scale device
+ * f32 [H] raw; w_in [H][64], w_out [64][H] device f32. The hidden state
+ * lives in the workspace (>= qi21_workspace_bytes(g, nseq*n)). */
+int qi21_denoise_batch(const qi21_geom* g, const qi21_layer* layers,
+                       const qi21_kvcache* const* caches, int32_t nseq, const float* tok,
+                       const float* w_in, const float* mods, const float* final_scale,
+                       const float* w_out, float* out, void* workspace, size_t ws_bytes,
+                       void* stream);
+
+/* qi21_denoise_batch for one sequence. */
+int qi21_denoise(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache,
+                 const float* tok, const float* w_in, const float* mods, const float* final_scale,
+                 const float* w_out, float* out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Size of the static device scratch behind qi21_step_noalloc: 32 MiB,
  * i.e. qi21_workspace_bytes(g, n) <= this bound (dim 4096 / mlp 12288: up to
  * 408 target rows; dim 256 / mlp 768: up to 6552). */
@@ -248,7 +286,9 @@ int qi21_device_status(void);
 #define QI21_CLASS_GATEUP 6    /* gate/up projection + SwiGLU */
 #define QI21_CLASS_DOWN 7      /* down projection + gated residual */
 #define QI21_CLASS_MISC 8      /* modulation prep */
-#define QI21_NCLASS 9
+#define QI21_CLASS_EMBED 9     /* image embedding (qi21_denoise) */
+#define QI21_CLASS_FINAL 10    /* final LN + proj_out (qi21_denoise) */
+#define QI21_NCLASS 11
 
 /* Per-class device timing of the passes, the analogue of the page's
  * per-class step times (gpu_wgpu/qi21.rs, class_times). on != 0 starts
