@@ -377,6 +377,44 @@ def denoise(tok, w_in, weights, mods, final_scale, w_out, segs, cache, cfg):
     return final_layer(x, final_scale, w_out, cfg["eps"])
 
 
+# ------------------------------------------------------------ timestep ----
+# qwen_image21.rs, Qi21Dit::temb and Qi21Dit::mods: the one shared modulation
+# of a denoiser call, from the model input t in [0, 1].
+
+TIMESTEP_CHANNELS = 256
+
+
+def timestep_sinusoid(t):
+    """[cos(a_i) | sin(a_i)], i < 128, a_i = (1000 t) f_i with
+    f_i = exp(-ln(10000) i / 128); every step in float32 as the page fixes
+    it (qwen_image21.rs, Qi21Dit::temb, the loop over HALF)."""
+    half = TIMESTEP_CHANNELS // 2
+    ts = np.float32(1000.0) * np.float32(t)
+    i = np.arange(half, dtype=np.float32)
+    f = np.exp(-np.log(np.float32(10000.0)) * i / np.float32(half))
+    a = ts * f
+    return np.concatenate([np.cos(a), np.sin(a)]).astype(np.float32)
+
+
+def linear_row(w, x):
+    """One vector through a bias-free nn.Linear [out, in]: f64 sums rounded
+    to f32 per output (qwen_image21.rs, lin_row)."""
+    return (np.asarray(w, dtype=np.float64) @ np.asarray(x, dtype=np.float64)).astype(np.float32)
+
+
+def timestep_embed(t, t_lin1, t_lin2):
+    """temb [dim] = t_lin2 silu(t_lin1 e(t)) (qwen_image21.rs, Qi21Dit::temb)."""
+    h = silu(linear_row(t_lin1, timestep_sinusoid(t)).astype(np.float64)).astype(np.float32)
+    return linear_row(t_lin2, h)
+
+
+def timestep_mods(t, t_lin1, t_lin2, modulation, norm_out):
+    """(mods [4 dim] raw [s1|g1|s2|g2], final_scale [dim]) of one timestep:
+    both read s = silu(temb) (qwen_image21.rs, Qi21Dit::mods)."""
+    s = silu(timestep_embed(t, t_lin1, t_lin2).astype(np.float64)).astype(np.float32)
+    return linear_row(modulation, s), linear_row(norm_out, s)
+
+
 def mods_dev(mods, h):
     """[s1 | tanh g1 | s2 | tanh g2]: the gate chunks tanh-ed in f32, the
     scale chunks as they are (qi21.rs, mods_dev)."""

@@ -21,7 +21,9 @@ Recipe (one stream per tensor, so any single tensor can be rebuilt alone):
 * per-head RMSNorm weights ``norm_q``, ``norm_k`` = 1 + N(0, 0.05) float32;
 * latent tokens ~ N(0, 1) float32 [n, 64]; img_in weight ~ N(0, 64^-1/2)
   and proj_out weight ~ N(0, dim^-1/2), float32 (the page keeps f32 copies
-  of both for its device path); final_scale ~ N(0, 0.1) float32.
+  of both for its device path); final_scale ~ N(0, 0.1) float32;
+* timestep weights t_lin1 [dim, 256], t_lin2 [dim, dim], modulation
+  [4 dim, dim], norm_out [dim, dim] ~ N(0, fan_in^-1/2) float32, no biases.
 """
 from __future__ import annotations
 
@@ -51,6 +53,10 @@ TAG_ID = {
     "w_in": 31,         # img_in
     "w_out": 32,        # proj_out
     "final_scale": 33,  # final modulation of norm_out
+    "t_lin1": 34,       # timestep_embedder.linear_1
+    "t_lin2": 35,       # timestep_embedder.linear_2
+    "modulation": 36,   # modulation.1
+    "norm_out": 37,     # norm_out.linear
     "op_test": 50,  # single-operation checks: index = a case number
 }
 
@@ -213,6 +219,17 @@ def w_out(w: Workload) -> np.ndarray:
 def final_scale(w: Workload) -> np.ndarray:
     """Final modulation (norm_out scale) of the step: float32 [dim], N(0, 0.1)."""
     return normal(w.seed, "final_scale", 0, w.dim, 0.1)
+
+
+TIMESTEP_CHANNELS = 256
+
+
+def timestep_weights(w: Workload) -> dict:
+    """t_lin1 [dim, 256], t_lin2 [dim, dim], modulation [4 dim, dim],
+    norm_out [dim, dim]: float32, N(0, fan_in^-1/2)."""
+    d = w.dim
+    shapes = {"t_lin1": (d, TIMESTEP_CHANNELS), "t_lin2": (d, d), "modulation": (4 * d, d), "norm_out": (d, d)}
+    return {k: normal(w.seed, k, 0, r * c, c ** -0.5).reshape(r, c) for k, (r, c) in shapes.items()}
 
 
 def mods0(w: Workload) -> np.ndarray:

@@ -7,6 +7,7 @@ import os
 
 import numpy as np
 import pytest
+from scipy import special as sp_special
 
 from oracle import qi21_oracle as O
 
@@ -461,3 +462,83 @@ def test_denoise_composes_embed_step_final():
         x, _, _ = O.block(x, W, mt, *O.target_rope(segs, cfg["axes"], cfg["theta"]), cfg, cache[l], None)
     want = O.layer_norm(x, cfg["eps"]) * (1 + fsc) @ w_out.T
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------- timestep pins --
+# qwen_image21.rs, Qi21Dit::temb / Qi21Dit::mods.
+
+def test_timestep_sinusoid_at_zero_and_closed_form():
+    # t = 0: every angle is 0, so the cos half is 1 and the sin half 0 exactly
+    e0 = O.timestep_sinusoid(0.0)
+    assert e0.shape == (256,) and e0.dtype == np.float32
+    np.testing.assert_array_equal(e0, np.r_[np.ones(128), np.zeros(128)].astype(np.float32))
+    # t = 0.001 gives 1000 t = 1: frequency i is 10000^(-i/128), a geometric
+    # ladder from 1 down to 10000^(-127/128); cos first, then sin
+    e = O.timestep_sinusoid(0.001).astype(np.float64)
+    f = np.array([10000.0 ** (-i / 128.0) for i in range(128)])
+    np.testing.assert_allclose(e[:128], np.cos(f), atol=2e-6)
+    np.testing.assert_allclose(e[128:], np.sin(f), atol=2e-6)
+    assert abs(e[0] - 0.5403023058681398) < 1e-6 and abs(e[128] - 0.8414709848078965) < 1e-6
+    # the unit circle, per frequency, at any t
+    for t in (0.0, 0.37, 1.0):
+        v = O.timestep_sinusoid(t).astype(np.float64)
+        np.testing.assert_allclose(v[:128] ** 2 + v[128:] ** 2, 1.0, atol=1e-6)
+    # at t = 1 the slowest frequency is 10000^(-127/128) (angle ~0.1075 rad)
+    v = O.timestep_sinusoid(1.0).astype(np.float64)
+    a = 1000.0 * 10000.0 ** (-127 / 128)
+    assert abs(v[127] - np.cos(a)) < 1e-5 and abs(v[255] - np.sin(a)) < 1e-5
+
+
+def _perm(n, seed):
+    p = np.random.default_rng(seed).permutation(n)
+    m = np.zeros((n, n), np.float32)
+    m[np.arange(n), p] = 1.0
+    return m, p
+
+
+def _silu_ref(v):
+    v = np.asarray(v, np.float64)
+    return v * sp_special.expit(v)
+
+
+def test_timestep_mods_through_permutations():
+    # with permutation weights every linear is a gather, so the result has a
+    # closed form: mods chunk c = (c + 1) silu(silu(silu(e)[p1])[p2])[p3]
+    # where the weights pick columns p; a transposed weight would apply the
+    # inverse permutation and fail
+    dim = 256
+    P1, p1 = _perm(dim, 1)
+    P2, p2 = _perm(dim, 2)
+    P3, p3 = _perm(dim, 3)
+    mod = np.concatenate([(c + 1) * P3 for c in range(4)]).astype(np.float32)
+    nout = (-2.0 * P2).astype(np.float32)
+    t = 0.731
+    e = O.timestep_sinusoid(t).astype(np.float64)
+    temb = _silu_ref(e[p1])[p2]
+    s = _silu_ref(temb)
+    mods, fs = O.timestep_mods(t, P1, P2, mod, nout)
+    np.testing.assert_allclose(O.timestep_embed(t, P1, P2), temb, rtol=1e-6, atol=1e-7)
+    for c in range(4):
+        np.testing.assert_allclose(mods[c * dim:(c + 1) * dim], (c + 1) * s[p3], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(fs, -2.0 * s[p2], rtol=1e-6, atol=1e-7)
+
+
+def test_timestep_mods_brute_force_tiny():
+    # dim 4: plain Python sums over the 256 sinusoid channels
+    rng = np.random.default_rng(5)
+    dim = 4
+    W1 = rng.standard_normal((dim, 256)).astype(np.float32) / 16
+    W2 = rng.standard_normal((dim, dim)).astype(np.float32)
+    Wm = rng.standard_normal((4 * dim, dim)).astype(np.float32)
+    Wn = rng.standard_normal((dim, dim)).astype(np.float32)
+    t = 0.25
+    e = [float(v) for v in O.timestep_sinusoid(t)]
+    sl = lambda v: v / (1.0 + math.exp(-v))
+    h = [sl(math.fsum(float(W1[r, k]) * e[k] for k in range(256))) for r in range(dim)]
+    temb = [math.fsum(float(W2[r, k]) * h[k] for k in range(dim)) for r in range(dim)]
+    s = [sl(v) for v in temb]
+    mods = [math.fsum(float(Wm[r, k]) * s[k] for k in range(dim)) for r in range(4 * dim)]
+    fs = [math.fsum(float(Wn[r, k]) * s[k] for k in range(dim)) for r in range(dim)]
+    got_m, got_f = O.timestep_mods(t, W1, W2, Wm, Wn)
+    np.testing.assert_allclose(got_m, mods, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(got_f, fs, rtol=1e-5, atol=1e-6)
