@@ -18,7 +18,7 @@ from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_T
 __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
-    "denoise", "denoise_batch", "device_status", "build",
+    "timestep_mods", "denoise", "set_checks", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -182,6 +182,41 @@ def final(x, final_scale, w_out, out, eps=1e-6, stream=None):
     check(load().qi21_final(x.shape[0], x.shape[1], w_out.shape[0], eps, _ptr(x, f, "x"),
                             _ptr(final_scale, f, "final_scale"), _ptr(w_out, f, "w_out"), _ptr(out, f, "out"),
                             _stream(stream)))
+
+
+CHECK_FINITE = 1
+
+
+def set_checks(flags: int) -> int:
+    """qi21_set_checks: process-wide optional checks (CHECK_FINITE); returns
+    the previous flags."""
+    return int(load().qi21_set_checks(int(flags)))
+
+
+def count_nonfinite(x, stream=None) -> int:
+    """qi21_count_nonfinite: NaN/Inf count of a CUDA f32 or f16 tensor
+    (synchronises the stream)."""
+    torch = _torch()
+    eb = {torch.float32: 4, torch.float16: 2}.get(x.dtype)
+    if eb is None:
+        raise TypeError("count_nonfinite takes f32 or f16 tensors")
+    out = C.c_uint64(0)
+    check(load().qi21_count_nonfinite(_ptr(x, x.dtype, "x"), x.numel(), eb, C.byref(out), _stream(stream)))
+    return int(out.value)
+
+
+def timestep_mods(t, t_lin1, t_lin2, modulation, norm_out, mods, final_scale, work=None, stream=None):
+    """qi21_timestep_mods: mods [4 dim] and final_scale [dim] of the model
+    input t (f32 weights t_lin1 [dim, 256], t_lin2, modulation, norm_out)."""
+    torch = _torch()
+    f = torch.float32
+    dim = t_lin2.shape[0]
+    if work is None:
+        work = torch.empty(2 * dim, dtype=f, device=mods.device)
+    check(load().qi21_timestep_mods(dim, float(t), _ptr(t_lin1, f, "t_lin1"), _ptr(t_lin2, f, "t_lin2"),
+                                    _ptr(modulation, f, "modulation"), _ptr(norm_out, f, "norm_out"),
+                                    _ptr(work, f, "work"), _ptr(mods, f, "mods"),
+                                    _ptr(final_scale, f, "final_scale"), _stream(stream)))
 
 
 def denoise_batch(g: Geom, layers, caches, tok, w_in, mods, final_scale, w_out, out, workspace, stream=None):

@@ -20,7 +20,7 @@ OK = 0
 ERR = {
     -1: "QI21_ERR_ARG", -2: "QI21_ERR_SHAPE", -3: "QI21_ERR_GEOM", -4: "QI21_ERR_MASK",
     -5: "QI21_ERR_OOM", -6: "QI21_ERR_CUDA", -7: "QI21_ERR_STATE", -8: "QI21_ERR_WORKSPACE",
-    -9: "QI21_ERR_DEVICE",
+    -9: "QI21_ERR_DEVICE", -10: "QI21_ERR_NONFINITE",
 }
 SEG_TEXT = 0
 SEG_IMAGE = 1
@@ -74,6 +74,9 @@ _SIGS = {
                                   _vp, _vp, _sz, _vp]),
     "qi21_embed": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "qi21_final": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
+    "qi21_set_checks": (C.c_uint32, [C.c_uint32]),
+    "qi21_count_nonfinite": (C.c_int, [_vp, C.c_size_t, _i32, C.POINTER(C.c_uint64), _vp]),
+    "qi21_timestep_mods": (C.c_int, [_i32, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_denoise_batch": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), C.POINTER(_vp), _i32, _vp, _vp, _vp, _vp,
                                      _vp, _vp, _vp, _sz, _vp]),
     "qi21_denoise": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -168,7 +171,7 @@ def device_status() -> int:
     return load().qi21_device_status()
 
 
-CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc", "embed", "final")
+CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc", "embed", "final", "temb")
 
 
 def profile_enable(on: bool) -> None:

@@ -629,9 +629,47 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b) {
   return QI21_OK;
 }
 
+std::atomic<uint32_t> g_checks{0};
+std::mutex g_count_mu;
+
+int count_bad(const void* x, size_t count, int eb, unsigned long long* bad, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_count_mu);
+  QI21_CK(count_nonfinite(x, count, eb, bad, s), "finite check");
+  return QI21_OK;
+}
+
+// The QI21_CHECK_FINITE refusal of what a pass wrote (no-op when off).
+int finite_check(const void* x, size_t count, int eb, const char* what, cudaStream_t s) {
+  if (!(g_checks.load(std::memory_order_relaxed) & QI21_CHECK_FINITE)) return QI21_OK;
+  unsigned long long bad = 0;
+  const int rc = count_bad(x, count, eb, &bad, s);
+  if (rc != QI21_OK) return rc;
+  if (bad) return fail(QI21_ERR_NONFINITE, "%s holds %llu non-finite values", what, bad);
+  return QI21_OK;
+}
+
+// qi21_step_batch without the finite check (qi21_denoise_batch checks the
+// velocity instead).
+int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
+                    const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
+                    size_t ws_bytes, void* stream);
+
 }  // namespace
 
 extern "C" {
+
+uint32_t qi21_set_checks(uint32_t flags) { return g_checks.exchange(flags); }
+
+int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64_t* out_count, void* stream) {
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(QI21_ERR_ARG, "elem_bytes %d (2 or 4)", elem_bytes);
+  if (out_count == nullptr || (count > 0 && x == nullptr)) return fail(QI21_ERR_ARG, "null pointer");
+  if (reinterpret_cast<uintptr_t>(x) % elem_bytes) return fail(QI21_ERR_ARG, "x not aligned to its element");
+  unsigned long long bad = 0;
+  const int rc = count_bad(x, count, elem_bytes, &bad, static_cast<cudaStream_t>(stream));
+  if (rc != QI21_OK) return rc;
+  *out_count = bad;
+  return QI21_OK;
+}
 
 int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cache,
                  const float* x_prefix, const float* mods0, float* x_layers, void* workspace,
@@ -653,13 +691,27 @@ int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cac
     QI21_CK(launch_mods_prep(g->dim, mods0, b.md, s), "mods prep");
   }
   rc = run_pass(g, layers, M, true, cache, nullptr, 1, 0, b, x_layers, s);
-  if (rc == QI21_OK) cache->filled = true;
-  return rc;
+  if (rc != QI21_OK) return rc;
+  cache->filled = true;
+  return finite_check(cache->kv, static_cast<size_t>(g->layers) * M * 2 * H, 2, "the K/V cache", s);
 }
 
 int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
                     int32_t nseq, const float* x_in, float* x_out, const float* mods, float* x_layers,
                     void* workspace, size_t ws_bytes, void* stream) {
+  const int rc = step_batch_impl(g, layers, caches, nseq, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream);
+  if (rc != QI21_OK) return rc;
+  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, 4, "the hidden state",
+                      static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
+                    const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
+                    size_t ws_bytes, void* stream) {
   int rc = geom_check(g);
   if (rc != QI21_OK) return rc;
   if (caches == nullptr || x_in == nullptr || x_out == nullptr || mods == nullptr)
@@ -691,6 +743,10 @@ int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
   return run_pass(g, layers, M, false, nullptr, caches, nseq, n, b, x_layers, s);
 }
 
+}  // namespace
+
+extern "C" {
+
 int qi21_embed(int32_t n, int32_t dim, int32_t in_ch, const float* tok, const float* w_in, float* x,
                void* stream) {
   if (n < 0 || dim <= 0 || dim % 4) return fail(QI21_ERR_SHAPE, "n %d dim %d", n, dim);
@@ -720,6 +776,22 @@ int qi21_final(int32_t n, int32_t dim, int32_t out_ch, float eps, const float* x
   return QI21_OK;
 }
 
+int qi21_timestep_mods(int32_t dim, float t, const float* t_lin1, const float* t_lin2, const float* modulation,
+                       const float* norm_out, float* work, float* mods, float* final_scale, void* stream) {
+  if (dim < 4 || dim % 4 || dim > 8192) return fail(QI21_ERR_SHAPE, "dim %d", dim);
+  if (!std::isfinite(t)) return fail(QI21_ERR_ARG, "t is not finite");
+  if (!t_lin1 || !t_lin2 || !modulation || !norm_out || !work || !mods || !final_scale)
+    return fail(QI21_ERR_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(t_lin1) | reinterpret_cast<uintptr_t>(t_lin2) |
+       reinterpret_cast<uintptr_t>(modulation) | reinterpret_cast<uintptr_t>(norm_out) |
+       reinterpret_cast<uintptr_t>(work)) % 16)
+    return fail(QI21_ERR_ARG, "weights and work must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(QI21_CLASS_TEMB, s);
+  QI21_CK(launch_timestep(dim, t, t_lin1, t_lin2, modulation, norm_out, work, mods, final_scale, s), "timestep");
+  return QI21_OK;
+}
+
 int qi21_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
                        int32_t nseq, const float* tok, const float* w_in, const float* mods,
                        const float* final_scale, const float* w_out, float* out, void* workspace,
@@ -743,10 +815,13 @@ int qi21_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_
     if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
   }
   if ((rc = qi21_embed(M, g->dim, QI21_LATENT_CHANNELS, tok, w_in, b.x, stream)) != QI21_OK) return rc;
-  if ((rc = qi21_step_batch(g, layers, caches, nseq, b.x, b.x, mods, nullptr, workspace, ws_bytes, stream)) !=
+  if ((rc = step_batch_impl(g, layers, caches, nseq, b.x, b.x, mods, nullptr, workspace, ws_bytes, stream)) !=
       QI21_OK)
     return rc;
-  return qi21_final(M, g->dim, QI21_LATENT_CHANNELS, g->eps, b.x, final_scale, w_out, out, stream);
+  if ((rc = qi21_final(M, g->dim, QI21_LATENT_CHANNELS, g->eps, b.x, final_scale, w_out, out, stream)) != QI21_OK)
+    return rc;
+  return finite_check(out, static_cast<size_t>(M) * QI21_LATENT_CHANNELS, 4, "the velocity",
+                      static_cast<cudaStream_t>(stream));
 }
 
 int qi21_denoise(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* cache, const float* tok,

@@ -44,6 +44,11 @@ cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half
 // x[n][dim] = tok[n][64] w_in[dim][64]^T (f32)
 cudaError_t launch_embed(int n, int dim, const float* tok, const float* w_in, float* x, cudaStream_t s);
 // out[n][64] = (LN(x)(1 + fs)) w_out[64][dim]^T (f32)
+cudaError_t launch_timestep(int dim, float t, const float* t_lin1, const float* t_lin2, const float* modulation,
+                            const float* norm_out, float* work, float* mods, float* final_scale, cudaStream_t s);
+// Synchronous: zeroes the counter, scans on s, reads it back, syncs s.
+// elem_bytes 4 (f32) or 2 (f16); x aligned to elem_bytes.
+cudaError_t count_nonfinite(const void* x, size_t count, int elem_bytes, unsigned long long* out, cudaStream_t s);
 cudaError_t launch_final(int n, int dim, float eps, const float* x, const float* fs, const float* w_out,
                          float* out, cudaStream_t s);
 

@@ -4,6 +4,8 @@
 // gpu_wgpu/qi21.rs, zi_embed and zi_final). Both projections have 64
 // latent channels on one side, so they are small f32 contractions run on
 // the CUDA cores (f32 weights, as the page keeps for its device path).
+// Also the timestep conditioning (qwen_image21.rs, Qi21Dit::temb and
+// Qi21Dit::mods): matrix-vector products, bound by reading the f32 weights.
 #include <algorithm>
 
 #include "internal.h"
@@ -153,6 +155,169 @@ cudaError_t launch_final(int n, int dim, float eps, const float* x, const float*
   if (n <= 0) return cudaSuccess;
   final_kernel<<<(n + kFinRows - 1) / kFinRows, 256, 0, s>>>(n, dim, eps, x, fs, w_out, out);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ timestep ----
+constexpr int kTsHalf = 128;  // the sinusoid has 2 * 128 channels
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+
+// h[r] = silu(sum_k t_lin1[r][k] e[k]) with e = [cos a_i | sin a_i],
+// a_i = (1000 t) exp(-ln(10000) i / 128), all in f32. One warp per row;
+// every CTA builds e in shared memory (128 exp + cos/sin pairs).
+__global__ void __launch_bounds__(256) temb_in_kernel(int dim, float t, const float* __restrict__ w1,
+                                                      float* __restrict__ h) {
+  __shared__ __align__(16) float e[2 * kTsHalf];
+  if (threadIdx.x < kTsHalf) {
+    const float ts = 1000.f * t;
+    const float f = expf(-logf(10000.f) * static_cast<float>(threadIdx.x) / static_cast<float>(kTsHalf));
+    const float a = ts * f;
+    e[threadIdx.x] = cosf(a);
+    e[kTsHalf + threadIdx.x] = sinf(a);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= dim) return;
+  const float4* w4 = reinterpret_cast<const float4*>(w1 + static_cast<size_t>(r) * 2 * kTsHalf);
+  const float4 a = __ldg(w4 + lane), b = __ldg(w4 + 32 + lane);
+  const float4 ea = reinterpret_cast<const float4*>(e)[lane], eb = reinterpret_cast<const float4*>(e)[32 + lane];
+  float acc = (a.x * ea.x + a.y * ea.y) + (a.z * ea.z + a.w * ea.w);
+  acc += (b.x * eb.x + b.y * eb.y) + (b.z * eb.z + b.w * eb.w);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) h[r] = silu_f(acc);
+}
+
+// y = W v over two stacked weight blocks (rows [0, ra) of wa into ya, then
+// rows [0, rb) of wb into yb), v = silu(x) if SILU else x, staged in shared
+// memory. One warp per output row, eight 16-byte loads in flight per lane.
+template <bool SILU>
+__global__ void __launch_bounds__(256) gemv_kernel(int ra, int rb, int cols, const float* __restrict__ wa,
+                                                   const float* __restrict__ wb, const float* __restrict__ x,
+                                                   float* __restrict__ ya, float* __restrict__ yb) {
+  extern __shared__ __align__(16) float v[];
+  for (int c = threadIdx.x; c < cols; c += 256) v[c] = SILU ? silu_f(x[c]) : x[c];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int r = blockIdx.x * 8 + warp;
+  if (r >= ra + rb) return;
+  const float* w = r < ra ? wa + static_cast<size_t>(r) * cols : wb + static_cast<size_t>(r - ra) * cols;
+  float* y = r < ra ? ya + r : yb + (r - ra);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  const float4* v4 = reinterpret_cast<const float4*>(v);
+  const int n4 = cols / 4;
+  float acc0 = 0.f, acc1 = 0.f;
+  int c = lane;
+  for (; c + 7 * 32 < n4; c += 8 * 32) {
+    float4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = __ldg(w4 + c + u * 32);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 z = v4[c + u * 32];
+      acc0 = fmaf(q[u].x, z.x, acc0);
+      acc1 = fmaf(q[u].y, z.y, acc1);
+      acc0 = fmaf(q[u].z, z.z, acc0);
+      acc1 = fmaf(q[u].w, z.w, acc1);
+    }
+  }
+  for (; c < n4; c += 32) {
+    const float4 q = __ldg(w4 + c), z = v4[c];
+    acc0 = fmaf(q.x, z.x, acc0);
+    acc1 = fmaf(q.y, z.y, acc1);
+    acc0 = fmaf(q.z, z.z, acc0);
+    acc1 = fmaf(q.w, z.w, acc1);
+  }
+  float acc = acc0 + acc1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) *y = acc;
+}
+
+cudaError_t launch_timestep(int dim, float t, const float* t_lin1, const float* t_lin2, const float* modulation,
+                            const float* norm_out, float* work, float* mods, float* final_scale,
+                            cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(dim) * 4;
+  float* h = work;
+  float* temb = work + dim;
+  temb_in_kernel<<<(dim + 7) / 8, 256, 0, s>>>(dim, t, t_lin1, h);
+  gemv_kernel<false><<<(dim + 7) / 8, 256, smem, s>>>(dim, 0, dim, t_lin2, nullptr, h, temb, nullptr);
+  gemv_kernel<true><<<(5 * dim + 7) / 8, 256, smem, s>>>(4 * dim, dim, dim, modulation, norm_out, temb, mods,
+                                                         final_scale);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- finite check ----
+// Counts NaN/Inf values by their exponent bits (all ones), so no floating
+// point is involved: f32 0x7f800000, f16 0x7c00. 16-byte loads over the
+// aligned body, scalar loads over the unaligned head and the tail; one
+// atomic per warp into a file-scope counter.
+static __device__ unsigned long long g_nonfinite;
+
+__global__ void zero_count_kernel() { g_nonfinite = 0ull; }
+
+template <int EB>
+__device__ __forceinline__ unsigned bad_elem(const uint8_t* p) {
+  if (EB == 4) return (*reinterpret_cast<const uint32_t*>(p) & 0x7f800000u) == 0x7f800000u;
+  return (*reinterpret_cast<const uint16_t*>(p) & 0x7c00u) == 0x7c00u;
+}
+
+template <int EB>
+__global__ void __launch_bounds__(256) count_nonfinite_kernel(const uint8_t* __restrict__ x, size_t count,
+                                                              size_t head, size_t nvec) {
+  constexpr int kPer = 16 / EB;
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nth = static_cast<size_t>(gridDim.x) * blockDim.x;
+  unsigned bad = 0;
+  // elements [0, head) and [head + nvec * kPer, count) one by one
+  const size_t tail0 = head + nvec * kPer;
+  for (size_t i = tid; i < head + (count - tail0); i += nth) {
+    const size_t e = i < head ? i : tail0 + (i - head);
+    bad += bad_elem<EB>(x + e * EB);
+  }
+  const uint4* v = reinterpret_cast<const uint4*>(x + head * EB);
+  for (size_t i = tid; i < nvec; i += nth) {
+    const uint4 q = v[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (EB == 4) {
+        bad += (w[k] & 0x7f800000u) == 0x7f800000u;
+      } else {
+        bad += (w[k] & 0x7c00u) == 0x7c00u;
+        bad += (w[k] & 0x7c000000u) == 0x7c000000u;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(&g_nonfinite, static_cast<unsigned long long>(bad));
+}
+
+cudaError_t count_nonfinite(const void* x, size_t count, int elem_bytes, unsigned long long* out,
+                            cudaStream_t s) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x);
+  size_t head = ((16 - (a & 15)) & 15) / elem_bytes;
+  if (head > count) head = count;
+  const size_t nvec = (count - head) / (16 / elem_bytes);
+  const size_t work = nvec + head + 1;
+  const unsigned grid = static_cast<unsigned>(std::min<size_t>((work + 255) / 256, 152 * 8));
+  zero_count_kernel<<<1, 1, 0, s>>>();
+  if (count > 0) {
+    if (elem_bytes == 4)
+      count_nonfinite_kernel<4><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(x), count, head, nvec);
+    else
+      count_nonfinite_kernel<2><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(x), count, head, nvec);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  unsigned long long h = 0;
+  if ((e = cudaMemcpyFromSymbolAsync(&h, g_nonfinite, sizeof(h), 0, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  *out = h;
+  return cudaSuccess;
 }
 
 }  // namespace qi21

@@ -47,6 +47,7 @@ extern "C" {
 #define QI21_ERR_STATE (-7)     /* cache not prefilled / layer out of range */
 #define QI21_ERR_WORKSPACE (-8) /* workspace too small or misaligned */
 #define QI21_ERR_DEVICE (-9)    /* a kernel raised its status word (timeout) */
+#define QI21_ERR_NONFINITE (-10) /* the optional finite check found NaN/Inf */
 
 /* Segment kinds of a layout (qwen_image21.rs, enum Seg). */
 #define QI21_SEG_TEXT 0  /* a = number of text rows, b unused */
@@ -272,6 +273,49 @@ int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers,
                     float* x_out, const float* mods, float* x_layers, void* workspace,
                     size_t ws_bytes, void* stream);
 
+#define QI21_TIMESTEP_CHANNELS 256
+
+/* Bytes of the `work` scratch of qi21_timestep_mods: 2 * dim floats. */
+#define QI21_TIMESTEP_WORK_BYTES(dim) ((size_t)(dim) * 8u)
+
+/* The one shared modulation of a denoiser call from the model input t
+ * (qwen_image21.rs, Qi21Dit::temb and Qi21Dit::mods; the page's pipeline
+ * passes t = timestep / 1000, and the prefix's modulation is t = 0):
+ *   e    = [cos a_i | sin a_i], a_i = 1000 t exp(-ln(10000) i / 128), i < 128
+ *   temb = t_lin2 silu(t_lin1 e),   s = silu(temb)
+ *   mods = modulation s  (raw [s1|g1|s2|g2], the input of qi21_step,
+ *                         qi21_prefill and qi21_denoise),
+ *   final_scale = norm_out s  (the input of qi21_final / qi21_denoise).
+ * No biases. Device f32 weights in nn.Linear layout, 16-byte aligned:
+ * t_lin1 [dim][256], t_lin2 [dim][dim], modulation [4 dim][dim], norm_out
+ * [dim][dim]. work: device scratch of QI21_TIMESTEP_WORK_BYTES(dim) (h, temb
+ * afterwards). Outputs mods f32 [4 dim], final_scale f32 [dim] (device;
+ * must not overlap work or the weights). dim % 4 == 0, 4 <= dim <= 8192.
+ * f32 arithmetic on the device (the page sums in f64 on the host). */
+int qi21_timestep_mods(int32_t dim, float t, const float* t_lin1, const float* t_lin2,
+                       const float* modulation, const float* norm_out, float* work, float* mods,
+                       float* final_scale, void* stream);
+
+/* Optional checks (process-wide flags). QI21_CHECK_FINITE is the page's
+ * non-finite decline (gpu_wgpu/qi21.rs, step: a velocity with a NaN or an
+ * infinity is refused, e.g. after an f16 overflow): with it set,
+ * qi21_prefill scans the cache's K/V, qi21_step / qi21_step_batch the
+ * hidden state x_out and qi21_denoise / qi21_denoise_batch the velocity
+ * after the pass, synchronise the stream and return QI21_ERR_NONFINITE if
+ * any value is NaN or infinite. The device buffers keep what was computed
+ * (the pass already ran); the return code is the refusal. Off by default:
+ * nothing synchronises. Do not set it while capturing a CUDA graph.
+ * Returns the previous flags. */
+#define QI21_CHECK_FINITE 1u
+uint32_t qi21_set_checks(uint32_t flags);
+
+/* Number of NaN/infinite values among `count` device elements of x (f32
+ * when elem_bytes == 4, f16 when 2; x aligned to its element). Enqueues the
+ * scan on stream, synchronises the stream and writes the count to
+ * *out_count (host). Calls from several host threads are serialised. */
+int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64_t* out_count,
+                         void* stream);
+
 /* Reads and clears the device status word (0 = fine; nonzero = a kernel
  * gave up waiting). Synchronises the device. */
 int qi21_device_status(void);
@@ -288,7 +332,8 @@ int qi21_device_status(void);
 #define QI21_CLASS_MISC 8      /* modulation prep */
 #define QI21_CLASS_EMBED 9     /* image embedding (qi21_denoise) */
 #define QI21_CLASS_FINAL 10    /* final LN + proj_out (qi21_denoise) */
-#define QI21_NCLASS 11
+#define QI21_CLASS_TEMB 11     /* timestep conditioning (qi21_timestep_mods) */
+#define QI21_NCLASS 12
 
 /* Per-class device timing of the passes, the analogue of the page's
  * per-class step times (gpu_wgpu/qi21.rs, class_times). on != 0 starts
