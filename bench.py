@@ -447,33 +447,46 @@ def run_gpu(args):
     fractions["gemm_frac"] = (fractions["gemm_tflops"] or 0) / peaks["bf16_tflops_sustained"]
     fractions["attention_frac"] = (fractions["attention_tflops"] or 0) / peaks["bf16_tflops_sustained"]
 
-    # the whole denoiser call of the pages (tokens -> embed -> blocks ->
-    # final -> velocity), timed on its own beside the step metric
+    # the whole sampler call of the pages (t -> modulation; tokens -> embed
+    # -> blocks -> final -> velocity), timed on its own beside the step metric
     denoise = None
     if not args.no_e2e:
+        tw = {k: torch.from_numpy(v).cuda() for k, v in S.timestep_weights(w).items()}
+        mods_c = torch.empty(4 * w.dim, device="cuda")
+        fs_c = torch.empty(w.dim, device="cuda")
+        t_work = torch.empty(2 * w.dim, device="cuda")
+
+        def sampler_call(t):
+            q.timestep_mods(t, tw["t_lin1"], tw["t_lin2"], tw["modulation"], tw["norm_out"], mods_c, fs_c,
+                            work=t_work)
+            q.denoise_batch(dw.g, dw.layers, dw.caches, tok, w_in, mods_c, fs_c, w_out, vel, dw.ws)
+
         tok = torch.from_numpy(S.tokens(w)).cuda()
         if w.nseq > 1:
             tok = tok.repeat(w.nseq, 1).contiguous()
         w_in = torch.from_numpy(S.w_in(w)).cuda()
         w_out = torch.from_numpy(S.w_out(w)).cuda()
-        fsc = torch.from_numpy(S.final_scale(w)).cuda()
         vel = torch.empty((n_rows, 64), device="cuda")
-        for _ in range(2):
-            q.denoise_batch(dw.g, dw.layers, dw.caches, tok, w_in, dw.mods_t, fsc, w_out, vel, dw.ws)
+        for i in range(2):
+            sampler_call(0.9 - 0.1 * i)
         q.profile_enable(True)
         torch.cuda.synchronize()
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         d0.record(stream)
         nd = max(2, args.steps // 2)
-        for _ in range(nd):
-            q.denoise_batch(dw.g, dw.layers, dw.caches, tok, w_in, dw.mods_t, fsc, w_out, vel, dw.ws)
+        for i in range(nd):
+            sampler_call(0.7 - 0.5 * i / nd)
         d1.record(stream)
         torch.cuda.synchronize()
         dms, _ = q.profile_read()
         q.profile_enable(False)
         ms = d0.elapsed_time(d1) / nd
+        temb_ms = dms["temb"] / nd
+        temb_bytes = 4.0 * sum(v.numel() for v in tw.values())
         denoise = {"ms": ms, "rows_per_s": n_rows / (ms * 1e-3), "calls": nd,
-                   "embed_ms": dms["embed"] / nd, "final_ms": dms["final"] / nd}
+                   "what": "timestep_mods + embed + step over all blocks + final, per call",
+                   "embed_ms": dms["embed"] / nd, "final_ms": dms["final"] / nd, "temb_ms": temb_ms,
+                   "temb_gbs": temb_bytes / (temb_ms * 1e-3) / 1e9 if temb_ms else None}
         if q.device_status() != 0:
             raise RuntimeError("a kernel gave up waiting during the denoiser calls")
 
