@@ -18,7 +18,7 @@ from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_T
 __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
-    "timestep_mods", "denoise", "set_checks", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
+    "timestep_mods", "denoise", "set_checks", "Graph", "graph_step_batch", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -182,6 +182,59 @@ def final(x, final_scale, w_out, out, eps=1e-6, stream=None):
     check(load().qi21_final(x.shape[0], x.shape[1], w_out.shape[0], eps, _ptr(x, f, "x"),
                             _ptr(final_scale, f, "final_scale"), _ptr(w_out, f, "w_out"), _ptr(out, f, "out"),
                             _stream(stream)))
+
+
+class Graph:
+    """A recorded step or denoiser call (qi21_graph_*): replay with
+    ``launch``. Bound to the tensors given at capture, which it keeps
+    alive; change their contents, not their storage."""
+
+    def __init__(self, handle, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        check(load().qi21_graph_launch(self.handle, _stream(stream)))
+
+    def free(self):
+        if self.handle:
+            load().qi21_graph_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def graph_step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace) -> Graph:
+    """qi21_graph_step_batch: record one step of every cache's sequence."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    h = C.c_void_p()
+    lay = _layer_array(layers)
+    check(load().qi21_graph_step_batch(C.byref(g), lay, arr, len(caches), _ptr(x_in, f, "x_in"),
+                                       _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"),
+                                       _ptr(workspace, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), C.byref(h)))
+    return Graph(h, (layers, caches, x_in, x_out, mods, workspace, lay))
+
+
+def graph_denoise_batch(g: Geom, layers, caches, tok, w_in, mods, final_scale, w_out, out, workspace) -> Graph:
+    """qi21_graph_denoise_batch: record one latent-tokens -> velocity call."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    h = C.c_void_p()
+    lay = _layer_array(layers)
+    check(load().qi21_graph_denoise_batch(C.byref(g), lay, arr, len(caches), _ptr(tok, f, "tok"),
+                                          _ptr(w_in, f, "w_in"), _ptr(mods, f, "mods"),
+                                          _ptr(final_scale, f, "final_scale"), _ptr(w_out, f, "w_out"),
+                                          _ptr(out, f, "out"), _ptr(workspace, None, "workspace"),
+                                          workspace.numel() * workspace.element_size(), C.byref(h)))
+    return Graph(h, (layers, caches, tok, w_in, mods, final_scale, w_out, out, workspace, lay))
 
 
 CHECK_FINITE = 1

@@ -75,6 +75,11 @@ _SIGS = {
     "qi21_embed": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "qi21_final": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
     "qi21_set_checks": (C.c_uint32, [C.c_uint32]),
+    "qi21_graph_step_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, C.c_size_t, C.POINTER(_vp)]),
+    "qi21_graph_denoise_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t,
+                                           C.POINTER(_vp)]),
+    "qi21_graph_launch": (C.c_int, [_vp, _vp]),
+    "qi21_graph_free": (None, [_vp]),
     "qi21_count_nonfinite": (C.c_int, [_vp, C.c_size_t, _i32, C.POINTER(C.c_uint64), _vp]),
     "qi21_timestep_mods": (C.c_int, [_i32, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_denoise_batch": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), C.POINTER(_vp), _i32, _vp, _vp, _vp, _vp,

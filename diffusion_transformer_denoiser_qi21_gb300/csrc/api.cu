@@ -83,11 +83,15 @@ static cudaEvent_t prof_event() {
 
 bool profiling_on() { return g_prof_on; }
 
+// Set while this thread records a graph (qi21_graph_*): no profiling events
+// and no synchronising checks go into a capture.
+static thread_local bool t_capturing = false;
+
 class ProfScope {
  public:
   ProfScope(int cls, cudaStream_t s) : cls_(cls), s_(s) {
     g_launches[cls].fetch_add(1, std::memory_order_relaxed);
-    if (!g_prof_on) return;
+    if (!g_prof_on || t_capturing) return;
     std::lock_guard<std::mutex> lk(g_prof_mu);
     a_ = prof_event();
     if (a_) cudaEventRecord(a_, s_);
@@ -640,7 +644,7 @@ int count_bad(const void* x, size_t count, int eb, unsigned long long* bad, cuda
 
 // The QI21_CHECK_FINITE refusal of what a pass wrote (no-op when off).
 int finite_check(const void* x, size_t count, int eb, const char* what, cudaStream_t s) {
-  if (!(g_checks.load(std::memory_order_relaxed) & QI21_CHECK_FINITE)) return QI21_OK;
+  if (t_capturing || !(g_checks.load(std::memory_order_relaxed) & QI21_CHECK_FINITE)) return QI21_OK;
   unsigned long long bad = 0;
   const int rc = count_bad(x, count, eb, &bad, s);
   if (rc != QI21_OK) return rc;
@@ -839,6 +843,97 @@ int qi21_step(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* 
   const qi21_kvcache* cs[1] = {cache};
   if (cache == nullptr) return fail(QI21_ERR_ARG, "null cache");
   return qi21_step_batch(g, layers, cs, 1, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream);
+}
+
+// ------------------------------------------------------------ graphs ----
+// A recorded call: the launches of one qi21_step_batch / qi21_denoise_batch
+// captured into a CUDA graph on a private stream (no profiling events, no
+// synchronising checks inside), then replayed as one graph launch.
+
+}  // extern "C"
+
+struct qi21_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+namespace {
+
+template <class F>
+int capture_graph(F&& record, qi21_graph** out) {
+  if (out == nullptr) return fail(QI21_ERR_ARG, "null output");
+  *out = nullptr;
+  cudaStream_t cs = nullptr;
+  QI21_CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking), "capture stream");
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "begin capture");
+  }
+  t_capturing = true;
+  const int rc = record(static_cast<void*>(cs));
+  t_capturing = false;
+  cudaGraph_t gr = nullptr;
+  e = cudaStreamEndCapture(cs, &gr);
+  cudaStreamDestroy(cs);
+  if (rc != QI21_OK) {
+    if (gr) cudaGraphDestroy(gr);
+    return rc;
+  }
+  if (e != cudaSuccess) {
+    if (gr) cudaGraphDestroy(gr);
+    return cuda_fail(e, "end capture");
+  }
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, gr, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(gr);
+    return cuda_fail(e, "graph instantiate");
+  }
+  auto* gg = new qi21_graph();
+  gg->graph = gr;
+  gg->exec = ex;
+  *out = gg;
+  return QI21_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qi21_graph_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
+                          int32_t nseq, const float* x_in, float* x_out, const float* mods, void* workspace,
+                          size_t ws_bytes, qi21_graph** out) {
+  return capture_graph(
+      [&](void* cs) {
+        return qi21_step_batch(g, layers, caches, nseq, x_in, x_out, mods, nullptr, workspace, ws_bytes, cs);
+      },
+      out);
+}
+
+int qi21_graph_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
+                             int32_t nseq, const float* tok, const float* w_in, const float* mods,
+                             const float* final_scale, const float* w_out, float* out_v, void* workspace,
+                             size_t ws_bytes, qi21_graph** out) {
+  return capture_graph(
+      [&](void* cs) {
+        return qi21_denoise_batch(g, layers, caches, nseq, tok, w_in, mods, final_scale, w_out, out_v, workspace,
+                                  ws_bytes, cs);
+      },
+      out);
+}
+
+int qi21_graph_launch(const qi21_graph* gr, void* stream) {
+  if (gr == nullptr || gr->exec == nullptr) return fail(QI21_ERR_ARG, "null graph");
+  QI21_CK(cudaGraphLaunch(gr->exec, static_cast<cudaStream_t>(stream)), "graph launch");
+  return QI21_OK;
+}
+
+void qi21_graph_free(qi21_graph* gr) {
+  if (gr == nullptr) return;
+  if (gr->exec) cudaGraphExecDestroy(gr->exec);
+  if (gr->graph) cudaGraphDestroy(gr->graph);
+  delete gr;
 }
 
 // ------------------------------------------------------ single operations --

@@ -316,6 +316,32 @@ uint32_t qi21_set_checks(uint32_t flags);
 int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64_t* out_count,
                          void* stream);
 
+/* A recorded call (this library's addition: the page replays command
+ * buffers it records once per prompt, gpu_wgpu/qi21.rs, Prog and
+ * run_calls). qi21_graph_step_batch / qi21_graph_denoise_batch validate
+ * their arguments exactly as qi21_step_batch / qi21_denoise_batch, then
+ * record that call's launches into a CUDA graph (on a private stream; the
+ * caller's streams are untouched, nothing runs); qi21_graph_launch replays
+ * it on `stream` as one launch. The graph is bound to every pointer given
+ * at capture (weights, caches, x / tokens, mods, final_scale, output,
+ * workspace): between launches the caller may change the contents of those
+ * buffers (new hidden states, the next timestep's mods) but not their
+ * addresses, and must keep them alive until qi21_graph_free. Replays take
+ * no profiling records and no finite checks; launches on one stream run in
+ * order, and graphs sharing a workspace must not overlap in time. */
+typedef struct qi21_graph qi21_graph;
+int qi21_graph_step_batch(const qi21_geom* g, const qi21_layer* layers,
+                          const qi21_kvcache* const* caches, int32_t nseq, const float* x_in,
+                          float* x_out, const float* mods, void* workspace, size_t ws_bytes,
+                          qi21_graph** out);
+int qi21_graph_denoise_batch(const qi21_geom* g, const qi21_layer* layers,
+                             const qi21_kvcache* const* caches, int32_t nseq, const float* tok,
+                             const float* w_in, const float* mods, const float* final_scale,
+                             const float* w_out, float* out_velocity, void* workspace,
+                             size_t ws_bytes, qi21_graph** out);
+int qi21_graph_launch(const qi21_graph* graph, void* stream);
+void qi21_graph_free(qi21_graph* graph);
+
 /* Reads and clears the device status word (0 = fine; nonzero = a kernel
  * gave up waiting). Synchronises the device. */
 int qi21_device_status(void);
