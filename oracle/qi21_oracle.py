@@ -223,7 +223,7 @@ def attention(q, k, v, visible, heads, head_dim):
 
 # ---------------------------------------------------------------- block ----
 
-def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None):
+def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None, lin=None):
     """One block on the query rows of x (qwen_image21.rs, Qi21Dit::block_cpu):
 
         xn = LN(x) (1 + s1); q, k, v = xn Wq^T, xn Wk^T, xn Wv^T
@@ -242,6 +242,9 @@ def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None):
     restricted to these rows (each output row depends only on its own
     query and on all keys).
 
+    lin: the projection a -> a W^T (default: the plain product; the FP8
+    variant passes linear_fp8).
+
     Returns (x_out [len(rows) or M, H], k [M, H], v [M, H]) with k, v the
     block's own post-RoPE keys and values."""
     H, nh, hd, eps = cfg["dim"], cfg["heads"], cfg["head_dim"], cfg["eps"]
@@ -251,10 +254,12 @@ def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None):
     s1, g1, s2, g2 = mods[:H], mods[H:2 * H], mods[2 * H:3 * H], mods[3 * H:]
     M = x.shape[0]
     sel = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    if lin is None:
+        lin = lambda a, w: a @ f(w).T  # noqa: E731
     xn = norm_mod(x, s1, eps)
-    k = qk_norm_rope(xn @ f(W["wk"]).T, W["norm_k"], cos, sin, nh, hd, eps)
-    v = xn @ f(W["wv"]).T
-    q = qk_norm_rope(xn[sel] @ f(W["wq"]).T, W["norm_q"], f(cos)[sel], f(sin)[sel], nh, hd, eps)
+    k = qk_norm_rope(lin(xn, W["wk"]), W["norm_k"], cos, sin, nh, hd, eps)
+    v = lin(xn, W["wv"])
+    q = qk_norm_rope(lin(xn[sel], W["wq"]), W["norm_q"], f(cos)[sel], f(sin)[sel], nh, hd, eps)
     if kv_prefix is not None:
         ka = np.concatenate([f(kv_prefix[0]), k], axis=0)
         va = np.concatenate([f(kv_prefix[1]), v], axis=0)
@@ -265,10 +270,10 @@ def block(x, W, mods, cos, sin, cfg, kv_prefix=None, visible=None, rows=None):
     else:
         vis = np.asarray(visible, dtype=np.int64)[sel]
     o = attention(q, ka, va, vis, nh, hd)
-    xs = gated_add(x[sel], o @ f(W["wo"]).T, g1)
+    xs = gated_add(x[sel], lin(o, W["wo"]), g1)
     xn2 = norm_mod(xs, s2, eps)
-    hid = silu(xn2 @ f(W["wgate"]).T) * (xn2 @ f(W["wup"]).T)
-    xs = gated_add(xs, hid @ f(W["wdown"]).T, g2)
+    hid = silu(lin(xn2, W["wgate"])) * lin(xn2, W["wup"])
+    xs = gated_add(xs, lin(hid, W["wdown"]), g2)
     return xs, k, v
 
 
@@ -278,7 +283,7 @@ def cfg_of(w) -> dict:
             "axes": tuple(w.axes), "theta": w.theta}
 
 
-def prefill(x_prefix, weights, mods0, segs, cfg, keep_x=False):
+def prefill(x_prefix, weights, mods0, segs, cfg, keep_x=False, lin=None):
     """The prefix through every block with the t = 0 modulation and the
     block-causal mask, keeping each layer's own post-RoPE (K, V)
     (qwen_image21.rs, Qi21Dit::prefill, host loop).
@@ -294,14 +299,14 @@ def prefill(x_prefix, weights, mods0, segs, cfg, keep_x=False):
     x = np.asarray(x_prefix, dtype=np.float64)
     cache, xs = [], []
     for W in weights:
-        x, k, v = block(x, W, mods0, cos, sin, cfg, None, vis)
+        x, k, v = block(x, W, mods0, cos, sin, cfg, None, vis, lin=lin)
         cache.append((k, v))
         if keep_x:
             xs.append(x)
     return cache, xs
 
 
-def step(x_target, weights, mods, segs, cache, cfg, keep_x=False):
+def step(x_target, weights, mods, segs, cache, cfg, keep_x=False, lin=None):
     """The target rows through every block against [cached prefix, own rows]
     with every key visible (qwen_image21.rs, Qi21Dit::step_cpu, the block
     loop; the image embedding and the final projection are outside it).
@@ -314,7 +319,7 @@ def step(x_target, weights, mods, segs, cache, cfg, keep_x=False):
     vis = np.full(n, lp + n, dtype=np.int64)
     xs = []
     for layer, W in enumerate(weights):
-        x, _, _ = block(x, W, mods, cos, sin, cfg, cache[layer], vis)
+        x, _, _ = block(x, W, mods, cos, sin, cfg, cache[layer], vis, lin=lin)
         if keep_x:
             xs.append(x)
     return x, xs
@@ -413,6 +418,87 @@ def timestep_mods(t, t_lin1, t_lin2, modulation, norm_out):
     both read s = silu(temb) (qwen_image21.rs, Qi21Dit::mods)."""
     s = silu(timestep_embed(t, t_lin1, t_lin2).astype(np.float64)).astype(np.float32)
     return linear_row(modulation, s), linear_row(norm_out, s)
+
+
+# ----------------------------------------------------------------- FP8 ----
+# A generic W8A8 variant of the four projections. The pages' device weights
+# are 8- and 4-bit codecs whose formats they do not give, so this variant
+# uses the OCP FP8 E4M3 format: every activation row and every weight row
+# (output channel) is scaled by a power of two so that its largest
+# magnitude fits 448, rounded to the nearest E4M3 value (ties to even,
+# saturating), multiplied as codes with wide accumulation, and the two
+# scales applied to the product. Powers of two keep scaling exact, so the
+# rounding decision depends only on the value being quantised.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one E4M3 byte (OCP FP8): sign bit 7, exponent bits 3..6
+    with bias 7, mantissa bits 0..2; exponent 0 is subnormal (m 2^-9);
+    0x7F / 0xFF are NaN, there is no infinity."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_grid():
+    """(values, codes) of the 127 finite non-negative E4M3 values, in
+    increasing order (codes 0x00 .. 0x7E)."""
+    codes = np.arange(0x7F, dtype=np.int64)
+    vals = np.array([e4m3_value(c) for c in codes], dtype=np.float64)
+    return vals, codes
+
+
+_E4M3_VALS, _E4M3_CODES = e4m3_grid()
+
+
+def round_e4m3(a):
+    """Round to the nearest E4M3 value, ties to the even code, magnitudes
+    beyond 448 saturating to 448 (the satfinite conversion)."""
+    a = np.asarray(a, dtype=np.float64)
+    m = np.minimum(np.abs(a), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_VALS, m, side="left"), 1, len(_E4M3_VALS) - 1)
+    lo = hi - 1
+    vlo, vhi = _E4M3_VALS[lo], _E4M3_VALS[hi]
+    dlo, dhi = m - vlo, vhi - m
+    take_hi = (dhi < dlo) | ((dhi == dlo) & (_E4M3_CODES[hi] % 2 == 0))
+    r = np.where(take_hi, vhi, vlo)
+    r = np.where(m == 0.0, 0.0, r)
+    return np.copysign(r, a)
+
+
+def pow2_exp(amax):
+    """Smallest integer e with amax <= 448 2^e (0 for amax = 0), from the
+    binary exponent of amax: amax = f 2^p with f in [0.5, 1) and
+    448 = 0.875 2^9."""
+    amax = np.asarray(amax, dtype=np.float64)
+    f, p = np.frexp(amax)
+    e = np.where(f <= 0.875, p - 9, p - 8)
+    return np.where(amax == 0.0, 0, e).astype(np.int64)
+
+
+def quantize_rows(a):
+    """(q, e): per row e = pow2_exp(max |a_row|) and q = round_e4m3(a 2^-e)
+    (E4M3 values as floats)."""
+    a = np.asarray(a, dtype=np.float64)
+    e = pow2_exp(np.max(np.abs(a), axis=-1))
+    q = round_e4m3(a * np.ldexp(1.0, -e)[..., None])
+    return q, e
+
+
+def linear_fp8(a, w):
+    """a W^T with both operands quantised row-wise (activation rows, weight
+    output channels): (q_a q_w^T) 2^(e_a + e_w)."""
+    qa, ea = quantize_rows(a)
+    qw, ew = quantize_rows(np.asarray(w, dtype=np.float64))
+    return (qa @ qw.T) * np.ldexp(1.0, ea[:, None] + ew[None, :])
 
 
 def mods_dev(mods, h):

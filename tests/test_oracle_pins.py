@@ -542,3 +542,73 @@ def test_timestep_mods_brute_force_tiny():
     got_m, got_f = O.timestep_mods(t, W1, W2, Wm, Wn)
     np.testing.assert_allclose(got_m, mods, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(got_f, fs, rtol=1e-5, atol=1e-6)
+
+
+# ------------------------------------------------------------ FP8 pins ----
+# OCP FP8 E4M3 (the generic 8-bit variant of the projections).
+
+def test_e4m3_decode_known_codes():
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+             0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in known.items():
+        assert O.e4m3_value(c) == v, hex(c)
+    assert math.isnan(O.e4m3_value(0x7F)) and math.isnan(O.e4m3_value(0xFF))
+    vals, codes = O.e4m3_grid()
+    assert len(vals) == 127 and np.all(np.diff(vals) > 0) and vals[-1] == 448.0
+    # 3 mantissa bits: 8 values per binade above the subnormals
+    assert np.sum((vals >= 1.0) & (vals < 2.0)) == 8
+
+
+def test_round_e4m3_ties_saturation_and_grid():
+    vals, _ = O.e4m3_grid()
+    # grid values are fixed points, with either sign
+    np.testing.assert_array_equal(O.round_e4m3(vals), vals)
+    np.testing.assert_array_equal(O.round_e4m3(-vals), -vals)
+    # ties go to the even code: 1.0625 between 1.0 (0x38) and 1.125 (0x39)
+    assert O.round_e4m3(1.0625) == 1.0
+    # 1.1875 between 1.125 (0x39) and 1.25 (0x3A)
+    assert O.round_e4m3(1.1875) == 1.25
+    # 2^-10 is halfway between 0 and the smallest subnormal 2^-9
+    assert O.round_e4m3(2.0 ** -10) == 0.0
+    assert O.round_e4m3(2.0 ** -10 * 1.0001) == 2.0 ** -9
+    # off a tie, the nearer neighbour
+    assert O.round_e4m3(1.0624) == 1.0 and O.round_e4m3(1.0626) == 1.125
+    # saturation (no infinity): everything beyond 448 clamps to 448
+    np.testing.assert_array_equal(O.round_e4m3([449.0, 464.0, 1e9, -1e9]), [448.0, 448.0, 448.0, -448.0])
+    # the result is always a grid value and the nearest one
+    rng = np.random.default_rng(0)
+    a = rng.standard_normal(20000) * np.exp2(rng.uniform(-12, 9, 20000))
+    r = O.round_e4m3(a)
+    assert np.all(np.isin(np.abs(r), vals))
+    best = np.min(np.abs(np.abs(a)[:, None] - vals[None, :]), axis=1)
+    inside = np.abs(a) <= 448.0
+    np.testing.assert_allclose(np.abs(np.abs(r) - np.abs(a))[inside], best[inside], rtol=0, atol=0)
+
+
+def test_pow2_exp_minimal():
+    assert O.pow2_exp(448.0) == 0 and O.pow2_exp(448.0000001) == 1
+    assert O.pow2_exp(224.0) == -1 and O.pow2_exp(1.0) == -8 and O.pow2_exp(0.0) == 0
+    rng = np.random.default_rng(1)
+    a = np.exp2(rng.uniform(-20, 20, 5000))
+    e = O.pow2_exp(a)
+    assert np.all(a <= 448.0 * np.exp2(e)) and np.all(a > 448.0 * np.exp2(e - 1.0))
+
+
+def test_linear_fp8_exact_on_grid_and_error_bound():
+    rng = np.random.default_rng(2)
+    vals, _ = O.e4m3_grid()
+    # rows already on the grid, each with one element at 448: no rounding,
+    # scale 1, so the product is the plain one
+    a = rng.choice(vals, size=(5, 33)) * rng.choice([-1.0, 1.0], size=(5, 33))
+    w = rng.choice(vals, size=(7, 33)) * rng.choice([-1.0, 1.0], size=(7, 33))
+    a[:, 0] = 448.0
+    w[:, 3] = -448.0
+    np.testing.assert_array_equal(O.linear_fp8(a, w), a @ w.T)
+    # scaling by powers of two commutes with quantisation
+    np.testing.assert_array_equal(O.linear_fp8(a * 8.0, w / 4.0), (a @ w.T) * 2.0)
+    # generic inputs: every element within half a grid step (relative 2^-4)
+    x = rng.standard_normal((16, 64))
+    q, e = O.quantize_rows(x)
+    deq = q * np.exp2(e)[:, None]
+    big = np.abs(x) >= 2.0 ** -6 * np.exp2(e)[:, None]
+    assert np.all(np.abs(deq - x)[big] <= np.abs(x)[big] * 2.0 ** -4 + 1e-300)
