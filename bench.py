@@ -42,6 +42,7 @@ def parse(argv=None):
     p.add_argument("--cpu-rows", type=int, default=0,
                    help="query rows of the CPU sample (0 = all target rows)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) variant leg")
     return p.parse_args(argv)
 
 
@@ -512,6 +513,46 @@ def run_gpu(args):
         if q.device_status() != 0:
             raise RuntimeError("a kernel gave up waiting during the denoiser calls")
 
+    # the FP8 (E4M3 W8A8) variant of the same step, reported beside the
+    # f16 headline (its own precision; not the metric's)
+    fp8 = None
+    if not args.no_fp8:
+        l8 = [q.pack_layer_fp8(dw.g, l) for l in dw.layers]
+        ws8 = torch.empty(q.workspace_bytes_fp8(dw.g, max([n_rows] + lp)), dtype=torch.uint8, device="cuda")
+        for s_, c_ in enumerate(dw.caches):
+            q.prefill_fp8(dw.g, l8, c_, dw.x_prefix[s_], dw.mods0, ws8)
+        out8 = torch.empty_like(dw.x_target)
+        for _ in range(args.warmup):
+            q.step_batch_fp8(dw.g, l8, dw.caches, dw.x_target, out8, dw.mods_t, ws8)
+        q.profile_enable(True)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            q.step_batch_fp8(dw.g, l8, dw.caches, dw.x_target, out8, dw.mods_t, ws8)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        cms8, _ = q.profile_read()
+        q.profile_enable(False)
+        if q.device_status() != 0:
+            raise RuntimeError("a kernel gave up waiting during the FP8 steps")
+        ms8 = f0.elapsed_time(f1) / args.steps
+        fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+        g8 = {}
+        for k in ("qkv", "o", "gateup", "down"):
+            if cms8.get(k, 0) > 0:
+                tf = work[k][1] * launches.get(k, 0) / args.steps / (cms8[k] / args.steps * 1e-3) / 1e12
+                g8[k] = {"ms_per_step": cms8[k] / args.steps, "tflops": tf, "frac_of_fp8_peak": tf / fp8_peak}
+        gms8 = sum(v["ms_per_step"] for v in g8.values())
+        fp8 = {"ms_per_step": ms8, "rows_per_s": n_rows / (ms8 * 1e-3), "tflops": flops_step / (ms8 * 1e-3) / 1e12,
+               "gemm_tflops": gemm_f / (gms8 * 1e-3) / 1e12 if gms8 else None,
+               "fp8_peak": fp8_peak, "fp8_peak_source": "2 x measured bf16_tflops_sustained (nominal 4.5 / 2.25)",
+               "gemms": g8, "quant_ms_per_step": cms8.get("quant", 0.0) / args.steps,
+               "attention_ms_per_step": cms8.get("attention", 0.0) / args.steps,
+               "launch": "direct launches with per-launch events"}
+        del l8, ws8, out8
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rps, spent, desc = oracle_layer_sample(w, args.cpu_rows)
@@ -530,6 +571,7 @@ def run_gpu(args):
             "launch": {"timed": "one recorded CUDA graph per step (qi21_graph_step_batch)",
                        "direct_profiled_ms_per_step": direct_ms},
             "denoise": denoise,
+            "fp8": fp8,
             "setup_s": t_setup,
         }
         print(json.dumps(line), flush=True)

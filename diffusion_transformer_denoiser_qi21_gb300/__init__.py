@@ -18,7 +18,8 @@ from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_T
 __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
-    "timestep_mods", "denoise", "set_checks", "Graph", "graph_step_batch", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
+    "timestep_mods", "denoise", "set_checks", "PackedLayerFp8", "pack_layer_fp8", "workspace_bytes_fp8",
+    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -298,6 +299,87 @@ def step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace, x_layers=N
                                  _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _ptr(x_layers, f, "x_layers"),
                                  _ptr(workspace, None, "workspace"),
                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# --------------------------------------------------------- FP8 variant ----
+
+class PackedLayerFp8:
+    """One block's E4M3 planes and scales (qi21_pack_layer_fp8); keeps its
+    buffer and the f16 layer (for the norm weights) alive."""
+
+    def __init__(self, mem, src, cstruct):
+        self.mem = mem
+        self.src = src
+        self.c = cstruct
+
+
+def pack_layer_fp8(g: Geom, packed: PackedLayer, stream=None) -> PackedLayerFp8:
+    """qi21_pack_layer_fp8: packed f16 planes -> E4M3 planes + row scales."""
+    torch = _torch()
+    lib = load()
+    nbytes = lib.qi21_layer_fp8_bytes(C.byref(g))
+    if nbytes == 0:
+        check(lib.qi21_geom_check(C.byref(g)))
+    mem = torch.empty(nbytes, dtype=torch.uint8, device=packed.planes.device)
+    out = B.LayerFp8()
+    check(lib.qi21_pack_layer_fp8(C.byref(g), C.byref(packed.c), mem.data_ptr(), nbytes, C.byref(out),
+                                  _stream(stream)))
+    return PackedLayerFp8(mem, packed, out)
+
+
+def _layer8_array(layers):
+    arr = (B.LayerFp8 * len(layers))()
+    for i, l in enumerate(layers):
+        arr[i] = l.c
+    return arr
+
+
+def workspace_bytes_fp8(g: Geom, rows: int) -> int:
+    return int(load().qi21_workspace_bytes_fp8(C.byref(g), rows))
+
+
+def prefill_fp8(g: Geom, layers8, cache: KVCache, x_prefix, mods0, workspace, x_layers=None, stream=None):
+    """qi21_prefill_fp8."""
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_prefill_fp8(C.byref(g), _layer8_array(layers8), cache.handle, _ptr(x_prefix, f, "x_prefix"),
+                                  _ptr(mods0, f, "mods0"), _ptr(x_layers, f, "x_layers"),
+                                  _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+
+
+def step_batch_fp8(g: Geom, layers8, caches, x_in, x_out, mods, workspace, x_layers=None, stream=None):
+    """qi21_step_batch_fp8."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    check(load().qi21_step_batch_fp8(C.byref(g), _layer8_array(layers8), arr, len(caches), _ptr(x_in, f, "x_in"),
+                                     _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"), _ptr(x_layers, f, "x_layers"),
+                                     _ptr(workspace, None, "workspace"),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def op_quant_rows(a, q, qs, stream=None):
+    torch = _torch()
+    check(load().qi21_op_quant_rows(a.shape[0], a.shape[1], _ptr(a, torch.float16, "a"), _ptr(q, torch.uint8, "q"),
+                                    _ptr(qs, torch.float32, "qs"), _stream(stream)))
+
+
+def op_rowop_fp8(x, scale, xq, xs, eps=1e-6, stream=None):
+    torch = _torch()
+    f = torch.float32
+    check(load().qi21_op_rowop_fp8(x.shape[0], x.shape[1], eps, _ptr(x, f, "x"), _ptr(scale, f, "scale"),
+                                   _ptr(xq, torch.uint8, "xq"), _ptr(xs, f, "xs"), _stream(stream)))
+
+
+def op_gemm_fp8(epi, A, sa, Bw, sw, out, gate_t=None, stream=None):
+    torch = _torch()
+    f = torch.float32
+    M, K = A.shape
+    N = Bw.shape[0]
+    check(load().qi21_op_gemm_fp8(epi, M, N, K, _ptr(A, torch.uint8, "A"), _ptr(sa, f, "sa"),
+                                  _ptr(Bw, torch.uint8, "B"), _ptr(sw, f, "sw"), _ptr(out, None, "out"),
+                                  out.shape[1], _ptr(gate_t, f, "gate_t"), _stream(stream)))
 
 
 # ------------------------------------------------------- single operations --

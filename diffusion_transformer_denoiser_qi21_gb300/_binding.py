@@ -33,6 +33,12 @@ class Qi21Error(RuntimeError):
         self.code = code
 
 
+class LayerFp8(C.Structure):
+    _fields_ = [("wqkv", C.c_void_p), ("wo", C.c_void_p), ("w13", C.c_void_p), ("w2", C.c_void_p),
+                ("s_qkv", C.c_void_p), ("s_o", C.c_void_p), ("s_13", C.c_void_p), ("s_2", C.c_void_p),
+                ("norm_q", C.c_void_p), ("norm_k", C.c_void_p)]
+
+
 class Geom(C.Structure):
     _fields_ = [("dim", C.c_int32), ("heads", C.c_int32), ("head_dim", C.c_int32),
                 ("mlp_hidden", C.c_int32), ("layers", C.c_int32), ("axes", C.c_int32 * 3),
@@ -75,6 +81,14 @@ _SIGS = {
     "qi21_embed": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "qi21_final": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
     "qi21_set_checks": (C.c_uint32, [C.c_uint32]),
+    "qi21_layer_fp8_bytes": (C.c_size_t, [_vp]),
+    "qi21_workspace_bytes_fp8": (C.c_size_t, [_vp, _i32]),
+    "qi21_pack_layer_fp8": (C.c_int, [_vp, _vp, _vp, C.c_size_t, _vp, _vp]),
+    "qi21_prefill_fp8": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp]),
+    "qi21_step_batch_fp8": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp]),
+    "qi21_op_quant_rows": (C.c_int, [_i32, _i32, _vp, _vp, _vp, _vp]),
+    "qi21_op_rowop_fp8": (C.c_int, [_i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
+    "qi21_op_gemm_fp8": (C.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
     "qi21_graph_step_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, C.c_size_t, C.POINTER(_vp)]),
     "qi21_graph_denoise_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t,
                                            C.POINTER(_vp)]),
@@ -176,7 +190,7 @@ def device_status() -> int:
     return load().qi21_device_status()
 
 
-CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc", "embed", "final", "temb")
+CLASSES = ("rowop", "qkv", "qkrope", "kvcopy", "attention", "o", "gateup", "down", "misc", "embed", "final", "temb", "quant")
 
 
 def profile_enable(on: bool) -> None:

@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -37,6 +38,12 @@ static int cuda_fail(cudaError_t e, const char* what) {
   return fail(e == cudaErrorMemoryAllocation ? QI21_ERR_OOM : QI21_ERR_CUDA, "%s: %s", what,
               cudaGetErrorString(e));
 }
+
+#define QI21_CK(expr, what)                        \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
 
 int sm_count() {
   static int n = 0;
@@ -233,10 +240,12 @@ static int geom_check(const qi21_geom* g) {
 static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t x, xn, panel, att, hid, md, total;
+  size_t x, xn, panel, att, hid, md, q8, qs, total;
 };
 
-static WsLayout ws_layout(const qi21_geom* g, int rows) {
+// fp8: the E4M3 activation rows (one buffer [M][max(H, I)] shared by xn,
+// att and hid in turn) and their row scales, after the f16 layout.
+static WsLayout ws_layout(const qi21_geom* g, int rows, bool fp8 = false) {
   const size_t M = static_cast<size_t>(rows), H = g->dim, I = g->mlp_hidden;
   WsLayout w{};
   size_t off = 0;
@@ -252,6 +261,13 @@ static WsLayout ws_layout(const qi21_geom* g, int rows) {
   off = align256(off + M * I * 2);
   w.md = off;
   off = align256(off + 4 * H * 4);
+  w.q8 = w.qs = 0;
+  if (fp8) {
+    w.q8 = off;
+    off = align256(off + M * std::max(H, I));
+    w.qs = off;
+    off = align256(off + M * 4);
+  }
   w.total = off;
   return w;
 }
@@ -336,6 +352,18 @@ size_t qi21_workspace_bytes(const qi21_geom* g, int32_t max_rows) {
   return ws_layout(g, max_rows).total;
 }
 
+size_t qi21_workspace_bytes_fp8(const qi21_geom* g, int32_t max_rows) {
+  if (geom_check(g) != QI21_OK || max_rows < 0) return 0;
+  return ws_layout(g, max_rows, true).total;
+}
+
+size_t qi21_layer_fp8_bytes(const qi21_geom* g) {
+  if (geom_check(g) != QI21_OK) return 0;
+  const size_t H = g->dim, I = g->mlp_hidden;
+  return align256(3 * H * H) + align256(H * H) + align256(2 * I * H) + align256(H * I) + align256(3 * H * 4) +
+         align256(H * 4) + align256(2 * I * 4) + align256(H * 4);
+}
+
 int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const void* wv,
                     const void* wo, const void* wgate, const void* wup, const void* wdown,
                     const float* norm_q, const float* norm_k, void* planes, size_t plane_bytes,
@@ -372,6 +400,60 @@ int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const vo
   out->w2 = w2;
   out->norm_q = norm_q;
   out->norm_k = norm_k;
+  return QI21_OK;
+}
+
+int qi21_pack_layer_fp8(const qi21_geom* g, const qi21_layer* planes, void* mem, size_t bytes, qi21_layer_fp8* out,
+                        void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (!planes || !mem || !out) return fail(QI21_ERR_ARG, "null pointer");
+  if (!planes->wqkv || !planes->wo || !planes->w13 || !planes->w2 || !planes->norm_q || !planes->norm_k)
+    return fail(QI21_ERR_ARG, "null plane");
+  if (bytes < qi21_layer_fp8_bytes(g))
+    return fail(QI21_ERR_SHAPE, "fp8 plane buffer %zu bytes, need %zu", bytes, qi21_layer_fp8_bytes(g));
+  if (reinterpret_cast<uintptr_t>(mem) % 256) return fail(QI21_ERR_ARG, "mem must be 256-byte aligned");
+  const size_t H = g->dim, I = g->mlp_hidden;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* p = static_cast<uint8_t*>(mem);
+  auto take = [&](size_t n) {
+    uint8_t* r = p;
+    p += align256(n);
+    return r;
+  };
+  uint8_t* qkv = take(3 * H * H);
+  uint8_t* qo = take(H * H);
+  uint8_t* q13 = take(2 * I * H);
+  uint8_t* q2 = take(H * I);
+  float* sqkv = reinterpret_cast<float*>(take(3 * H * 4));
+  float* so = reinterpret_cast<float*>(take(H * 4));
+  float* s13 = reinterpret_cast<float*>(take(2 * I * 4));
+  float* s2 = reinterpret_cast<float*>(take(H * 4));
+  {
+    ProfScope ps(QI21_CLASS_QUANT, s);
+    QI21_CK(launch_quant_rows(static_cast<int>(3 * H), static_cast<int>(H), static_cast<const __half*>(planes->wqkv),
+                              H, qkv, H, sqkv, s),
+            "quantise wqkv");
+    QI21_CK(launch_quant_rows(static_cast<int>(H), static_cast<int>(H), static_cast<const __half*>(planes->wo), H, qo,
+                              H, so, s),
+            "quantise wo");
+    QI21_CK(launch_quant_rows(static_cast<int>(2 * I), static_cast<int>(H), static_cast<const __half*>(planes->w13),
+                              H, q13, H, s13, s),
+            "quantise w13");
+    QI21_CK(launch_quant_rows(static_cast<int>(H), static_cast<int>(I), static_cast<const __half*>(planes->w2), I, q2,
+                              I, s2, s),
+            "quantise w2");
+  }
+  out->wqkv = qkv;
+  out->wo = qo;
+  out->w13 = q13;
+  out->w2 = q2;
+  out->s_qkv = sqkv;
+  out->s_o = so;
+  out->s_13 = s13;
+  out->s_2 = s2;
+  out->norm_q = planes->norm_q;
+  out->norm_k = planes->norm_k;
   return QI21_OK;
 }
 
@@ -505,11 +587,21 @@ int check_layers(const qi21_geom* g, const qi21_layer* layers) {
   return QI21_OK;
 }
 
-#define QI21_CK(expr, what)                        \
-  do {                                             \
-    cudaError_t e_ = (expr);                       \
-    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
-  } while (0)
+int check_layers_fp8(const qi21_geom* g, const qi21_layer_fp8* layers) {
+  if (layers == nullptr) return fail(QI21_ERR_ARG, "null layers");
+  for (int l = 0; l < g->layers; ++l) {
+    const qi21_layer_fp8& w = layers[l];
+    if (!w.wqkv || !w.wo || !w.w13 || !w.w2 || !w.s_qkv || !w.s_o || !w.s_13 || !w.s_2 || !w.norm_q || !w.norm_k)
+      return fail(QI21_ERR_ARG, "layer %d: null plane", l);
+    if ((reinterpret_cast<uintptr_t>(w.wqkv) | reinterpret_cast<uintptr_t>(w.wo) |
+         reinterpret_cast<uintptr_t>(w.w13) | reinterpret_cast<uintptr_t>(w.w2) | reinterpret_cast<uintptr_t>(w.s_qkv) |
+         reinterpret_cast<uintptr_t>(w.s_o) | reinterpret_cast<uintptr_t>(w.s_13) | reinterpret_cast<uintptr_t>(w.s_2)) %
+        16)
+      return fail(QI21_ERR_ARG, "layer %d: planes and scales must be 16-byte aligned", l);
+  }
+  return QI21_OK;
+}
+
 
 // One layer's second half: attention -> O (+gate) -> LN2 -> gate/up -> down
 // (+gate); the first half (LN1, qkv, qkrope) is done by the caller.
@@ -520,11 +612,17 @@ struct PassBufs {
   __half* att;
   __half* hid;
   float* md;
+  uint8_t* q8;  // FP8 pass: E4M3 activation rows (xn, att, hid in turn)
+  float* qs;    // FP8 pass: their row scales
 };
 
-int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
+// One pass over the layers. Exactly one of layers (f16 planes) and l8 (the
+// FP8 variant: E4M3 planes, every projection on row-quantised activations)
+// is non-null.
+int run_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8* l8, int M, bool prefill,
              qi21_kvcache* pcache, const qi21_kvcache* const* caches, int nseq, int n,
              const PassBufs& b, float* x_layers, cudaStream_t s) {
+  const bool f8 = l8 != nullptr;
   const int H = g->dim, I = g->mlp_hidden, L = g->layers;
   const float* s1 = b.md;
   const float* g1 = b.md + H;
@@ -540,19 +638,39 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
     for (int q = 0; q < nseq; ++q) tabs.src[q] = RopeSrc{caches[q]->cos_t, caches[q]->sin_t, q * n};
   }
 
-  {
+  // the modulated LayerNorm of x (f16 xn, or E4M3 rows + scales)
+  auto ln = [&](const float* scale) -> int {
     ProfScope ps(QI21_CLASS_ROWOP, s);
-    QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s1, b.xn, s), "rowop");
-  }
+    if (f8)
+      QI21_CK(launch_rowop_q8(M, H, g->eps, b.x, scale, b.q8, b.qs, s), "rowop q8");
+    else
+      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, scale, b.xn, s), "rowop");
+    return QI21_OK;
+  };
+  // f16 rows -> E4M3 rows + scales (FP8 pass: att and hid)
+  auto quant = [&](const __half* a, int cols) -> int {
+    ProfScope ps(QI21_CLASS_QUANT, s);
+    QI21_CK(launch_quant_rows(M, cols, a, static_cast<size_t>(cols), b.q8, static_cast<size_t>(cols), b.qs, s),
+            "quantise rows");
+    return QI21_OK;
+  };
+  int rc;
+  if ((rc = ln(s1)) != QI21_OK) return rc;
   for (int l = 0; l < L; ++l) {
-    const qi21_layer& w = layers[l];
     const bool last = (l + 1 == L);
+    const float* norm_q = f8 ? l8[l].norm_q : layers[l].norm_q;
+    const float* norm_k = f8 ? l8[l].norm_k : layers[l].norm_k;
     GemmPlan pq, po, p13, p2;
     // qkv projection with the qk RMSNorm + RoPE fused into its epilogue
-    QI21_CK(make_gemm_plan(&pq, EPI_QKV, M, 3 * H, H, b.xn, static_cast<const __half*>(w.wqkv),
-                           b.panel, 3 * H, nullptr),
-            "qkv plan");
-    pq.qkv = QkvEpi{w.norm_q, w.norm_k, g->eps, H, tabs};
+    if (f8)
+      QI21_CK(make_gemm_plan_f8(&pq, EPI_QKV, M, 3 * H, H, b.q8, b.qs, l8[l].wqkv, l8[l].s_qkv, b.panel, 3 * H,
+                                nullptr),
+              "qkv plan");
+    else
+      QI21_CK(make_gemm_plan(&pq, EPI_QKV, M, 3 * H, H, b.xn, static_cast<const __half*>(layers[l].wqkv), b.panel,
+                             3 * H, nullptr),
+              "qkv plan");
+    pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs};
     {
       ProfScope ps(QI21_CLASS_QKV, s);
       QI21_CK(launch_gemm(pq, s), "qkv gemm");
@@ -583,25 +701,36 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
       ProfScope ps(QI21_CLASS_ATTENTION, s);
       QI21_CK(launch_attention(aa, s), "attention");
     }
-    QI21_CK(make_gemm_plan(&po, EPI_RESID, M, H, H, b.att, static_cast<const __half*>(w.wo), b.x, H, g1),
-            "o plan");
+    if (f8) {
+      if ((rc = quant(b.att, H)) != QI21_OK) return rc;
+      QI21_CK(make_gemm_plan_f8(&po, EPI_RESID, M, H, H, b.q8, b.qs, l8[l].wo, l8[l].s_o, b.x, H, g1), "o plan");
+    } else {
+      QI21_CK(make_gemm_plan(&po, EPI_RESID, M, H, H, b.att, static_cast<const __half*>(layers[l].wo), b.x, H, g1),
+              "o plan");
+    }
     {
       ProfScope ps(QI21_CLASS_O, s);
       QI21_CK(launch_gemm(po, s), "o gemm");
     }
-    {
-      ProfScope ps(QI21_CLASS_ROWOP, s);
-      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s2, b.xn, s), "rowop");
-    }
-    QI21_CK(make_gemm_plan(&p13, EPI_SWIGLU, M, 2 * I, H, b.xn, static_cast<const __half*>(w.w13),
-                           b.hid, I, nullptr),
-            "w13 plan");
+    if ((rc = ln(s2)) != QI21_OK) return rc;
+    if (f8)
+      QI21_CK(make_gemm_plan_f8(&p13, EPI_SWIGLU, M, 2 * I, H, b.q8, b.qs, l8[l].w13, l8[l].s_13, b.hid, I, nullptr),
+              "w13 plan");
+    else
+      QI21_CK(make_gemm_plan(&p13, EPI_SWIGLU, M, 2 * I, H, b.xn, static_cast<const __half*>(layers[l].w13), b.hid, I,
+                             nullptr),
+              "w13 plan");
     {
       ProfScope ps(QI21_CLASS_GATEUP, s);
       QI21_CK(launch_gemm(p13, s), "gate/up gemm");
     }
-    QI21_CK(make_gemm_plan(&p2, EPI_RESID, M, H, I, b.hid, static_cast<const __half*>(w.w2), b.x, H, g2),
-            "down plan");
+    if (f8) {
+      if ((rc = quant(b.hid, I)) != QI21_OK) return rc;
+      QI21_CK(make_gemm_plan_f8(&p2, EPI_RESID, M, H, I, b.q8, b.qs, l8[l].w2, l8[l].s_2, b.x, H, g2), "down plan");
+    } else {
+      QI21_CK(make_gemm_plan(&p2, EPI_RESID, M, H, I, b.hid, static_cast<const __half*>(layers[l].w2), b.x, H, g2),
+              "down plan");
+    }
     {
       ProfScope ps(QI21_CLASS_DOWN, s);
       QI21_CK(launch_gemm(p2, s), "down gemm");
@@ -610,18 +739,15 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, int M, bool prefill,
       QI21_CK(cudaMemcpyAsync(x_layers + static_cast<size_t>(l) * M * H, b.x,
                               static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
               "x_layers copy");
-    if (!last) {
-      ProfScope ps(QI21_CLASS_ROWOP, s);
-      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, s1, b.xn, s), "rowop");
-    }
+    if (!last && (rc = ln(s1)) != QI21_OK) return rc;
   }
   return QI21_OK;
 }
 
-int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b) {
+int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, bool fp8 = false) {
   if (ws == nullptr) return fail(QI21_ERR_WORKSPACE, "null workspace");
   if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(QI21_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  const WsLayout w = ws_layout(g, M);
+  const WsLayout w = ws_layout(g, M, fp8);
   if (ws_bytes < w.total) return fail(QI21_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, w.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
   b->x = reinterpret_cast<float*>(base + w.x);
@@ -630,6 +756,8 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b) {
   b->att = reinterpret_cast<__half*>(base + w.att);
   b->hid = reinterpret_cast<__half*>(base + w.hid);
   b->md = reinterpret_cast<float*>(base + w.md);
+  b->q8 = fp8 ? base + w.q8 : nullptr;
+  b->qs = fp8 ? reinterpret_cast<float*>(base + w.qs) : nullptr;
   return QI21_OK;
 }
 
@@ -656,7 +784,32 @@ int finite_check(const void* x, size_t count, int eb, const char* what, cudaStre
 // velocity instead).
 int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
                     const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
-                    size_t ws_bytes, void* stream);
+                    size_t ws_bytes, void* stream, const qi21_layer_fp8* l8 = nullptr);
+
+int prefill_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8* l8, qi21_kvcache* cache,
+                 const float* x_prefix, const float* mods0, float* x_layers, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (cache == nullptr || x_prefix == nullptr || mods0 == nullptr) return fail(QI21_ERR_ARG, "null pointer");
+  if (!same_geom(*g, cache->g)) return fail(QI21_ERR_SHAPE, "the cache was made for another geometry");
+  if ((rc = l8 ? check_layers_fp8(g, l8) : check_layers(g, layers)) != QI21_OK) return rc;
+  const int M = cache->lp;
+  PassBufs b;
+  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b, l8 != nullptr)) != QI21_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t H = g->dim;
+  QI21_CK(cudaMemcpyAsync(b.x, x_prefix, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
+          "x copy");
+  {
+    ProfScope ps(QI21_CLASS_MISC, s);
+    QI21_CK(launch_mods_prep(g->dim, mods0, b.md, s), "mods prep");
+  }
+  rc = run_pass(g, l8 ? nullptr : layers, l8, M, true, cache, nullptr, 1, 0, b, x_layers, s);
+  if (rc != QI21_OK) return rc;
+  cache->filled = true;
+  return finite_check(cache->kv, static_cast<size_t>(g->layers) * M * 2 * H, 2, "the K/V cache", s);
+}
 
 }  // namespace
 
@@ -678,26 +831,24 @@ int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64
 int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cache,
                  const float* x_prefix, const float* mods0, float* x_layers, void* workspace,
                  size_t ws_bytes, void* stream) {
-  int rc = geom_check(g);
+  return prefill_impl(g, layers, nullptr, cache, x_prefix, mods0, x_layers, workspace, ws_bytes, stream);
+}
+
+int qi21_prefill_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, qi21_kvcache* cache, const float* x_prefix,
+                     const float* mods0, float* x_layers, void* workspace, size_t ws_bytes, void* stream) {
+  if (layers == nullptr && geom_check(g) == QI21_OK) return fail(QI21_ERR_ARG, "null layers");
+  return prefill_impl(g, nullptr, layers, cache, x_prefix, mods0, x_layers, workspace, ws_bytes, stream);
+}
+
+int qi21_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, const qi21_kvcache* const* caches,
+                        int32_t nseq, const float* x_in, float* x_out, const float* mods, float* x_layers,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  if (layers == nullptr && geom_check(g) == QI21_OK) return fail(QI21_ERR_ARG, "null layers");
+  const int rc =
+      step_batch_impl(g, nullptr, caches, nseq, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream, layers);
   if (rc != QI21_OK) return rc;
-  if (cache == nullptr || x_prefix == nullptr || mods0 == nullptr) return fail(QI21_ERR_ARG, "null pointer");
-  if (!same_geom(*g, cache->g)) return fail(QI21_ERR_SHAPE, "the cache was made for another geometry");
-  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
-  const int M = cache->lp;
-  PassBufs b;
-  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t H = g->dim;
-  QI21_CK(cudaMemcpyAsync(b.x, x_prefix, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
-          "x copy");
-  {
-    ProfScope ps(QI21_CLASS_MISC, s);
-    QI21_CK(launch_mods_prep(g->dim, mods0, b.md, s), "mods prep");
-  }
-  rc = run_pass(g, layers, M, true, cache, nullptr, 1, 0, b, x_layers, s);
-  if (rc != QI21_OK) return rc;
-  cache->filled = true;
-  return finite_check(cache->kv, static_cast<size_t>(g->layers) * M * 2 * H, 2, "the K/V cache", s);
+  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, 4, "the hidden state",
+                      static_cast<cudaStream_t>(stream));
 }
 
 int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
@@ -715,7 +866,7 @@ namespace {
 
 int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
                     const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
-                    size_t ws_bytes, void* stream) {
+                    size_t ws_bytes, void* stream, const qi21_layer_fp8* l8) {
   int rc = geom_check(g);
   if (rc != QI21_OK) return rc;
   if (caches == nullptr || x_in == nullptr || x_out == nullptr || mods == nullptr)
@@ -730,10 +881,10 @@ int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
     if (n < 0) n = c->n;
     if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
   }
-  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
+  if ((rc = l8 ? check_layers_fp8(g, l8) : check_layers(g, layers)) != QI21_OK) return rc;
   const int M = nseq * n;
   PassBufs b;
-  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
+  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b, l8 != nullptr)) != QI21_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t H = g->dim;
   if (x_out != x_in)
@@ -744,7 +895,7 @@ int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
     ProfScope ps(QI21_CLASS_MISC, s);
     QI21_CK(launch_mods_prep(g->dim, mods, b.md, s), "mods prep");
   }
-  return run_pass(g, layers, M, false, nullptr, caches, nseq, n, b, x_layers, s);
+  return run_pass(g, layers, l8, M, false, nullptr, caches, nseq, n, b, x_layers, s);
 }
 
 }  // namespace
@@ -972,6 +1123,47 @@ int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, co
                          ldo, gate_t),
           "gemm plan");
   QI21_CK(launch_gemm(p, static_cast<cudaStream_t>(stream)), "gemm");
+  return QI21_OK;
+}
+
+int qi21_op_quant_rows(int32_t rows, int32_t cols, const void* a, void* q, float* qs, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 8) return fail(QI21_ERR_SHAPE, "rows %d cols %d", rows, cols);
+  if (rows == 0) return QI21_OK;
+  if (!a || !q || !qs) return fail(QI21_ERR_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(q)) % 16)
+    return fail(QI21_ERR_ARG, "a and q must be 16-byte aligned");
+  QI21_CK(launch_quant_rows(rows, cols, static_cast<const __half*>(a), static_cast<size_t>(cols),
+                            static_cast<uint8_t*>(q), static_cast<size_t>(cols), qs, static_cast<cudaStream_t>(stream)),
+          "quantise rows");
+  return QI21_OK;
+}
+
+int qi21_op_rowop_fp8(int32_t rows, int32_t dim, float eps, const float* x, const float* scale, void* xq, float* xs,
+                      void* stream) {
+  if (rows < 0 || dim <= 0 || dim % 4 || dim > 8192) return fail(QI21_ERR_SHAPE, "rows %d dim %d", rows, dim);
+  if (rows == 0) return QI21_OK;
+  if (!x || !scale || !xq || !xs) return fail(QI21_ERR_ARG, "null pointer");
+  QI21_CK(launch_rowop_q8(rows, dim, eps, x, scale, static_cast<uint8_t*>(xq), xs, static_cast<cudaStream_t>(stream)),
+          "rowop q8");
+  return QI21_OK;
+}
+
+int qi21_op_gemm_fp8(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const float* sa, const void* B,
+                     const float* sw, void* out, int32_t ldo, const float* gate, void* stream) {
+  if (epi != EPI_F32 && epi != EPI_RESID && epi != EPI_SWIGLU) return fail(QI21_ERR_ARG, "epilogue %d", epi);
+  if (M < 0 || N <= 0 || K <= 0 || N % 256 || K % 128) return fail(QI21_ERR_SHAPE, "M %d N %d K %d", M, N, K);
+  if (M == 0) return QI21_OK;
+  if (!A || !sa || !B || !sw || !out || (epi == EPI_RESID && !gate)) return fail(QI21_ERR_ARG, "null pointer");
+  const int cols = epi == EPI_SWIGLU ? N / 2 : N;
+  if (ldo < cols || ldo % 8) return fail(QI21_ERR_SHAPE, "ldo %d", ldo);
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(out) |
+       reinterpret_cast<uintptr_t>(sw)) % 16)
+    return fail(QI21_ERR_ARG, "A, B, sw and out must be 16-byte aligned");
+  GemmPlan p;
+  QI21_CK(make_gemm_plan_f8(&p, epi, M, N, K, static_cast<const uint8_t*>(A), sa, static_cast<const uint8_t*>(B), sw,
+                            out, ldo, gate),
+          "gemm plan");
+  QI21_CK(launch_gemm(p, static_cast<cudaStream_t>(stream)), "gemm fp8");
   return QI21_OK;
 }
 

@@ -44,6 +44,12 @@ cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half
 // x[n][dim] = tok[n][64] w_in[dim][64]^T (f32)
 cudaError_t launch_embed(int n, int dim, const float* tok, const float* w_in, float* x, cudaStream_t s);
 // out[n][64] = (LN(x)(1 + fs)) w_out[64][dim]^T (f32)
+// E4M3 row quantisation (the FP8 variant): LN(x)(1 + scale) -> codes, and
+// f16 rows -> codes; xs / qs[row] = 2^e (dequantisation factor).
+cudaError_t launch_rowop_q8(int rows, int dim, float eps, const float* x, const float* scale, uint8_t* xq,
+                            float* xs, cudaStream_t s);
+cudaError_t launch_quant_rows(int rows, int cols, const __half* a, size_t lda, uint8_t* q, size_t ldq, float* qs,
+                              cudaStream_t s);
 cudaError_t launch_timestep(int dim, float t, const float* t_lin1, const float* t_lin2, const float* modulation,
                             const float* norm_out, float* work, float* mods, float* final_scale, cudaStream_t s);
 // Synchronous: zeroes the counter, scans on s, reads it back, syncs s.
@@ -74,11 +80,18 @@ struct GemmPlan {
   void* out;
   const float* gate;
   QkvEpi qkv;
+  bool f8;           // E4M3 operands (tensor maps of bytes, box 128 x rows)
+  const float* sa;   // FP8: per A row scale
+  const float* sw;   // FP8: per B row scale
 };
 
 // Encode the tensor maps of C = A B^T. Returns cudaSuccess or an error.
 cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
                            const __half* B, void* out, int ldo, const float* gate);
+// The FP8 form: A, B E4M3 codes [M][K], [N][K] (row pitch K bytes), the
+// accumulator scaled by sa[row] sw[col]; N % 256 == 0, K % 128 == 0.
+cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const uint8_t* A, const float* sa,
+                              const uint8_t* B, const float* sw, void* out, int ldo, const float* gate);
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s);
 
 // -------------------------------------------------------------- attention --

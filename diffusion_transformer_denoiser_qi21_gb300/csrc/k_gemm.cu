@@ -12,6 +12,12 @@
 //              whole 128-column head vectors of its row)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
+// The FP8 instance (F8 = true) runs the same pipeline on E4M3 operands:
+// byte-wide tensor maps with 128-byte boxes (128 elements per k-block, the
+// same swizzled 128-byte rows), tcgen05.mma.kind::f8f6f4 (K = 32), and the
+// accumulator multiplied by the A row scale and the B row (output channel)
+// scale, both powers of two, before the epilogue above.
+//
 // Persistent clusters of two CTAs (one per SM) running the pair MMA
 // (tcgen05.mma.cta_group::2, a 256 x BN tile per CTA pair): CTA r holds rows
 // [128 r, 128 r + 128) of the A tile and rows [BN/2 r, BN/2 r + BN/2) of
@@ -68,14 +74,33 @@ struct EpiArgs {
   int ldo;
   const float* gate;
   QkvEpi qkv;
+  const float* sa;  // FP8: per A row
+  const float* sw;  // FP8: per B row (output column)
 };
+
+// FP8: 32 accumulator columns starting at column `col` times sa sw[col + i]
+template <bool F8>
+__device__ __forceinline__ void f8_scale(uint32_t (&r)[32], float sa, const float* __restrict__ sw, int col) {
+  if constexpr (F8) {
+    const float4* s4 = reinterpret_cast<const float4*>(sw + col);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 w = __ldg(s4 + j);
+      r[4 * j + 0] = __float_as_uint(__uint_as_float(r[4 * j + 0]) * sa * w.x);
+      r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) * sa * w.y);
+      r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) * sa * w.z);
+      r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) * sa * w.w);
+    }
+  }
+}
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8>
 __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0, int bn,
                                               const EpiArgs& ep) {
   const bool live = row < M;
+  const float sa = (F8 && live) ? ep.sa[row] : 1.f;
   if constexpr (EPI == EPI_SWIGLU) {
     __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
 #pragma unroll 1
@@ -87,6 +112,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
         tmem_ld32(tbase + p * 128 + 64 + c * 32, u);
         tmem_ld_wait(g);
         tmem_ld_wait(u);
+        f8_scale<F8>(g, sa, ep.sw, n0 + p * 128 + c * 32);
+        f8_scale<F8>(u, sa, ep.sw, n0 + p * 128 + 64 + c * 32);
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(out + p * 64 + c * 32);
 #pragma unroll
@@ -125,6 +152,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
       if (!live) continue;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) f8_scale<F8>(r[c], sa, ep.sw, col + c * 32);
       uint4* dst = reinterpret_cast<uint4*>(out + col);
       if (part == 2) {
 #pragma unroll
@@ -180,6 +209,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
       tmem_ld_wait(r);
       if (!live) continue;
       const int col = n0 + c * 32;
+      f8_scale<F8>(r, sa, ep.sw, col);
       if constexpr (EPI == EPI_F16) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(ep.out) +
                                               static_cast<size_t>(row) * ep.ldo + col);
@@ -233,7 +263,7 @@ __device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nfull) {
   return TileInfo{tf % num_mp, (tf / num_mp) * BN + (u & 1) * (BN / 2), BN / 2};
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, int M, int N, int K, int nfull,
@@ -256,7 +286,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
   const int num_mp = ((M + kBM - 1) / kBM + 1) / 2;
-  const int nk = K / kBK;
+  constexpr int kKE = F8 ? 128 : kBK;  // K elements per k-block (128 bytes per row)
+  const int nk = K / kKE;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -304,8 +335,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           uint8_t* sa = smem + s * C::kStageBytes;
           const uint32_t fb = mapa_rank(&full[s], 0);
           if (leader) mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
-          tma_load_2d_pair(sa + C::kABytes, half ? &tmBh : &tmB, fb, kb * kBK, ti.n0 + rank * bh);
+          tma_load_2d_pair(sa, &tmA, fb, kb * kKE, m0);
+          tma_load_2d_pair(sa + C::kABytes, half ? &tmBh : &tmB, fb, kb * kKE, ti.n0 + rank * bh);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -338,8 +369,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t adesc = sdesc_sw128(sa);
           const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc_mma_f16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of each 128-byte row
+            if constexpr (F8)
+              tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              tc_mma_f16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
           tc_commit_pair(&empty[s], 0x3);
           if (++s == C::kStages) {
             s = 0;
@@ -359,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      gemm_epilogue<BN, EPI>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
+      gemm_epilogue<BN, EPI, F8>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_rank(&tempty[acc], 0));
@@ -390,16 +425,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D f16 tensor [outer][inner] with the given row pitch; box inner x outer.
+// 2-D f16 (or byte) tensor [outer][inner] with the given row pitch; box
+// inner x outer.
 static cudaError_t encode_f16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 bool bytes = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  const CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                        const_cast<void*>(ptr), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -415,6 +453,8 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   p->out = out;
   p->gate = gate;
   p->qkv = QkvEpi{};
+  p->f8 = false;
+  p->sa = p->sw = nullptr;
   p->bn = (N % 256 == 0) ? 256 : 128;
   cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
   if (e != cudaSuccess) return e;
@@ -425,12 +465,33 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4);
 }
 
-template <int BN, int EPI>
+cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const uint8_t* A, const float* sa,
+                              const uint8_t* B, const float* sw, void* out, int ldo, const float* gate) {
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->epi = epi;
+  p->ldo = ldo;
+  p->out = out;
+  p->gate = gate;
+  p->qkv = QkvEpi{};
+  p->f8 = true;
+  p->sa = sa;
+  p->sw = sw;
+  p->bn = 256;
+  cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K), 128, kBM, true);
+  if (e != cudaSuccess) return e;
+  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 2, true);
+  if (e != cudaSuccess) return e;
+  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, true);
+}
+
+template <int BN, int EPI, bool F8 = false>
 static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   using C = GemmCfg<BN>;
   static int max_clusters = 0;
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -438,7 +499,7 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, F8>, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters = n > 0 ? n : 1;
   }
@@ -452,14 +513,24 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     total = nfull + 2 * rem;
   }
   const int clusters = std::min(total, max_clusters);
-  EpiArgs ep{p.out, p.ldo, p.gate, p.qkv};
-  gemm_tc_kernel<BN, EPI><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull,
-                                                               total, ep);
+  EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw};
+  gemm_tc_kernel<BN, EPI, F8><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull,
+                                                                   total, ep);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
   if (p.M <= 0) return cudaSuccess;
+  if (p.f8) {
+    if (p.bn != 256) return cudaErrorInvalidValue;
+    switch (p.epi) {
+      case EPI_F32: return launch_t<256, EPI_F32, true>(p, s);
+      case EPI_RESID: return launch_t<256, EPI_RESID, true>(p, s);
+      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, true>(p, s);
+      case EPI_QKV: return launch_t<256, EPI_QKV, true>(p, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.bn == 256) {
     switch (p.epi) {
       case EPI_F16: return launch_t<256, EPI_F16>(p, s);

@@ -106,6 +106,129 @@ __global__ void __launch_bounds__(kRowThreads) rowop_kernel(int dim, float eps, 
   }
 }
 
+__device__ __forceinline__ float block_max_256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  return fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
+               fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+}
+
+// The modulated LayerNorm with an E4M3 output (the FP8 variant's xn): the
+// f32 row LN(x)(1 + scale) is scaled by 2^-e, e the row's power-of-two
+// exponent, and rounded to E4M3 codes; xs[row] = 2^e.
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) rowop_q8_kernel(int dim, float eps, const float* __restrict__ x,
+                                                               const float* __restrict__ scale,
+                                                               uint8_t* __restrict__ xq, float* __restrict__ xs) {
+  __shared__ float red[8];
+  const size_t row = blockIdx.x;
+  const int nv = dim >> 2;
+  const float4* x4 = reinterpret_cast<const float4*>(x + row * dim);
+  float4 v[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int idx = threadIdx.x + j * kRowThreads;
+    if (idx < nv) v[j] = x4[idx];
+  }
+  float sm = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+  const float mean = block_sum_256(sm, red) / static_cast<float>(dim);
+  float sq = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    if (threadIdx.x + j * kRowThreads < nv) {
+      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
+      sq += (a * a + b * b) + (c * c + d * d);
+    }
+  }
+  const float inv = rsqrtf(block_sum_256(sq, red) / static_cast<float>(dim) + eps);
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int idx = threadIdx.x + j * kRowThreads;
+    if (idx < nv) {
+      const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
+      v[j].x = (v[j].x - mean) * inv * (1.f + sc.x);
+      v[j].y = (v[j].y - mean) * inv * (1.f + sc.y);
+      v[j].z = (v[j].z - mean) * inv * (1.f + sc.z);
+      v[j].w = (v[j].w - mean) * inv * (1.f + sc.w);
+      am = fmaxf(am, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    }
+  }
+  const int e = e4m3_row_exp(block_max_256(am, red));
+  const float r = ldexpf(1.f, -e);
+  uint32_t* q4 = reinterpret_cast<uint32_t*>(xq + row * dim);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int idx = threadIdx.x + j * kRowThreads;
+    if (idx < nv) q4[idx] = e4m3x4(v[j].x * r, v[j].y * r, v[j].z * r, v[j].w * r);
+  }
+  if (threadIdx.x == 0) xs[row] = ldexpf(1.f, e);
+}
+
+cudaError_t launch_rowop_q8(int rows, int dim, float eps, const float* x, const float* scale, uint8_t* xq,
+                            float* xs, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int per = (dim / 4 + kRowThreads - 1) / kRowThreads;
+  if (per <= 1)
+    rowop_q8_kernel<1><<<rows, kRowThreads, 0, s>>>(dim, eps, x, scale, xq, xs);
+  else if (per <= 2)
+    rowop_q8_kernel<2><<<rows, kRowThreads, 0, s>>>(dim, eps, x, scale, xq, xs);
+  else if (per <= 4)
+    rowop_q8_kernel<4><<<rows, kRowThreads, 0, s>>>(dim, eps, x, scale, xq, xs);
+  else
+    rowop_q8_kernel<8><<<rows, kRowThreads, 0, s>>>(dim, eps, x, scale, xq, xs);
+  return cudaGetLastError();
+}
+
+// f16 rows -> E4M3 rows with a power-of-two scale per row (the FP8
+// variant's att, hid and weight planes): q = e4m3(a 2^-e), qs[row] = 2^e.
+// One 256-thread CTA per row, 8 halves per thread per step; the row is read
+// twice (the second pass mostly from L1).
+__global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(int cols, const __half* __restrict__ a, size_t lda,
+                                                                 uint8_t* __restrict__ q, size_t ldq,
+                                                                 float* __restrict__ qs) {
+  __shared__ float red[8];
+  const size_t row = blockIdx.x;
+  const uint4* a8 = reinterpret_cast<const uint4*>(a + row * lda);
+  const int n8 = cols >> 3;
+  float am = 0.f;
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    const uint4 u = a8[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+      am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  const int e = e4m3_row_exp(block_max_256(am, red));
+  const float r = ldexpf(1.f, -e);
+  uint2* q8 = reinterpret_cast<uint2*>(q + row * ldq);
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    const uint4 u = a8[i];
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&u.z));
+    const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
+    q8[i] = make_uint2(e4m3x4(f0.x * r, f0.y * r, f1.x * r, f1.y * r), e4m3x4(f2.x * r, f2.y * r, f3.x * r, f3.y * r));
+  }
+  if (threadIdx.x == 0) qs[row] = ldexpf(1.f, e);
+}
+
+cudaError_t launch_quant_rows(int rows, int cols, const __half* a, size_t lda, uint8_t* q, size_t ldq, float* qs,
+                              cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  quant_rows_kernel<<<rows, kRowThreads, 0, s>>>(cols, a, lda, q, ldq, qs);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
                          const float* scale, __half* xn, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;

@@ -227,6 +227,20 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
+// Pair MMA on E4M3 operands (kind::f8f6f4, K = 32 per instruction: the
+// same 32 bytes of a 128-byte swizzled row as K = 16 of f16), f32 D. The
+// instruction descriptor is idesc_f16's: E4M3 is type code 0 in both
+// operand fields.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, f16 inputs, f32 accumulator.
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -318,6 +332,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Four values to E4M3 codes (round to nearest even, saturating at 448),
+// value i in byte i.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Smallest integer e with amax <= 448 2^e (0 for amax = 0): with
+// amax = f 2^p, f in [0.5, 1), and 448 = 0.875 2^9, e = p - 9 if
+// f <= 0.875 else p - 8.
+__device__ __forceinline__ int e4m3_row_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int p;
+  const float f = frexpf(amax, &p);
+  return f <= 0.875f ? p - 9 : p - 8;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {

@@ -342,6 +342,60 @@ int qi21_graph_denoise_batch(const qi21_geom* g, const qi21_layer* layers,
 int qi21_graph_launch(const qi21_graph* graph, void* stream);
 void qi21_graph_free(qi21_graph* graph);
 
+/* ------------------------------------------------------- FP8 variant ---- */
+/* A generic W8A8 variant of the four projections (qkv, O, gate/up, down).
+ * The page's device weights are 8- and 4-bit codecs whose formats it does
+ * not give (gpu_wgpu/qi21.rs module notes), so this variant uses the OCP
+ * FP8 E4M3 format: every weight row (output channel) and every activation
+ * row entering a projection (xn, the attention output, the SwiGLU hidden
+ * row) is scaled by a power of two 2^-e, e the smallest integer with
+ * max|row| <= 448 2^e, and rounded to the nearest E4M3 value (ties to even,
+ * saturating); the tensor cores multiply the codes (kind::f8f6f4, f32
+ * accumulation) and the epilogue applies both scales. The attention, the
+ * norms, the residual stream and the K/V cache are as in the f16 path. Not
+ * the headline precision: its per-block error is set by the 3-bit mantissa
+ * (about 2^-5 relative per operand element), not by the f16 bar. */
+
+/* E4M3 planes of one layer: codes with the shapes of qi21_layer's planes
+ * (wqkv [3H][H], wo [H][H], w13 [2I][H] interleaved, w2 [H][I]) and one f32
+ * scale 2^e per row. */
+typedef struct qi21_layer_fp8 {
+  const uint8_t* wqkv;
+  const uint8_t* wo;
+  const uint8_t* w13;
+  const uint8_t* w2;
+  const float* s_qkv;
+  const float* s_o;
+  const float* s_13;
+  const float* s_2;
+  const float* norm_q;
+  const float* norm_k;
+} qi21_layer_fp8;
+
+/* Bytes of one layer's E4M3 planes + scales (256-byte aligned pieces). */
+size_t qi21_layer_fp8_bytes(const qi21_geom* g);
+
+/* Quantise a layer's packed f16 planes (from qi21_pack_layer) into `mem`
+ * (device, >= qi21_layer_fp8_bytes, 256-byte aligned; owned by the caller)
+ * and fill *out (norm_q/norm_k are taken over). Asynchronous on stream. */
+int qi21_pack_layer_fp8(const qi21_geom* g, const qi21_layer* planes, void* mem, size_t bytes,
+                        qi21_layer_fp8* out, void* stream);
+
+/* Workspace of the FP8 passes: the f16 layout plus one E4M3 row buffer
+ * [rows][max(H, I)] and its row scales. */
+size_t qi21_workspace_bytes_fp8(const qi21_geom* g, int32_t max_rows);
+
+/* qi21_prefill / qi21_step_batch with the FP8 projections; same arguments,
+ * layouts, errors and cache format (a cache prefilled either way can be
+ * stepped either way). workspace >= qi21_workspace_bytes_fp8. */
+int qi21_prefill_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, qi21_kvcache* cache,
+                     const float* x_prefix, const float* mods0, float* x_layers, void* workspace,
+                     size_t ws_bytes, void* stream);
+int qi21_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers,
+                        const qi21_kvcache* const* caches, int32_t nseq, const float* x_in,
+                        float* x_out, const float* mods, float* x_layers, void* workspace,
+                        size_t ws_bytes, void* stream);
+
 /* Reads and clears the device status word (0 = fine; nonzero = a kernel
  * gave up waiting). Synchronises the device. */
 int qi21_device_status(void);
@@ -359,7 +413,8 @@ int qi21_device_status(void);
 #define QI21_CLASS_EMBED 9     /* image embedding (qi21_denoise) */
 #define QI21_CLASS_FINAL 10    /* final LN + proj_out (qi21_denoise) */
 #define QI21_CLASS_TEMB 11     /* timestep conditioning (qi21_timestep_mods) */
-#define QI21_NCLASS 12
+#define QI21_CLASS_QUANT 12    /* E4M3 row quantisation (FP8 variant) */
+#define QI21_NCLASS 13
 
 /* Per-class device timing of the passes, the analogue of the page's
  * per-class step times (gpu_wgpu/qi21.rs, class_times). on != 0 starts
@@ -409,6 +464,19 @@ int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, co
  * (qwen_image21.rs, Qi21Dit::qk_norm_rope; gpu_wgpu/qi21.rs, zi_qkrope). */
 int qi21_op_qkrope(int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
                    const float* norm_k, const float* cos_, const float* sin_, void* stream);
+
+/* FP8 variant, single operations. qi21_op_quant_rows: f16 a [rows][cols]
+ * (cols % 8 == 0) -> E4M3 codes q [rows][cols] and qs[row] = 2^e.
+ * qi21_op_rowop_fp8: LN(x)(1 + scale) of f32 x [rows][dim] -> codes
+ * xq [rows][dim] and xs[row] = 2^e. qi21_op_gemm_fp8: acc = A B^T on codes
+ * A [M][K], B [N][K] (N % 256 == 0, K % 128 == 0), times sa[row] sw[col],
+ * then the epilogue (QI21_EPI_F32, _RESID or _SWIGLU, as qi21_op_gemm). */
+int qi21_op_quant_rows(int32_t rows, int32_t cols, const void* a, void* q, float* qs, void* stream);
+int qi21_op_rowop_fp8(int32_t rows, int32_t dim, float eps, const float* x, const float* scale,
+                      void* xq, float* xs, void* stream);
+int qi21_op_gemm_fp8(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const float* sa,
+                     const void* B, const float* sw, void* out, int32_t ldo, const float* gate,
+                     void* stream);
 
 /* cache f16 [rows][2H] = panel columns [H, 3H) (gpu_wgpu/qi21.rs,
  * qi_kvcopy). */
