@@ -76,6 +76,7 @@ struct GemmPlan {
   CUtensorMap tmA;  // A f16 [M][K], box 64 x 128, 128B swizzle
   CUtensorMap tmB;  // B f16 [N][K], box 64 x BN, 128B swizzle
   CUtensorMap tmBh; // B f16 [N][K], box 64 x BN/2 (split tiles of a partial last wave)
+  CUtensorMap tmX;  // EPI_RESID: x f32 [M][ldo], box 32 x 32, 128B swizzle
   int M, N, K, bn, epi, ldo;
   void* out;
   const float* gate;

@@ -3,7 +3,9 @@
 // f32 accumulation in TMEM, fused epilogues:
 //   EPI_F16    qkv panel store                (gpu_wgpu/qi21.rs, zi_mm f16)
 //   EPI_RESID  x += tanh(g) * acc on the f32 residual stream (the O and down
-//              projections followed by Qi21Dit::gated_add)
+//              projections followed by Qi21Dit::gated_add); x moves through
+//              shared memory in 32 x 32 chunks by TMA (load, update, store),
+//              double-buffered per epilogue warp
 //   EPI_SWIGLU silu(gate) * up on the interleaved gate/up plane
 //              (qwen_image21.rs, block_cpu: silu(gate) * proj)
 //   EPI_QKV    the qkv panel store with the per-head qk RMSNorm * w and the
@@ -58,15 +60,23 @@ unsigned int gemm_status_read_clear() {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
-template <int BN>
+
+template <int BN, int EPI>
 struct GemmCfg {
   static constexpr int kABytes = kBM * kBK * 2;        // this CTA's A rows
   static constexpr int kBBytes = (BN / 2) * kBK * 2;   // this CTA's half of B
   static constexpr int kStageBytes = kABytes + kBBytes;
+  // EPI_RESID: per epilogue warp a ring of kXBufs 32 x 32 f32 chunks of x
+  // (4 KB each; kXBufs - 1 loads ahead) beside the same 192 KB of operand
+  // stages (224 KB in all; four buffers with one stage fewer measured the
+  // same)
+  static constexpr int kXBufs = 2;
+  static constexpr int kEpiBytes = EPI == EPI_RESID ? 4 * kXBufs * 4096 : 0;
   static constexpr int kStages = (192 * 1024) / kStageBytes;
+  static constexpr int kEpiOff = kStages * kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
+  static constexpr int kSmem = kEpiOff + kEpiBytes + kBarBytes + 1024;
 };
 
 struct EpiArgs {
@@ -266,17 +276,18 @@ __device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nfull) {
 template <int BN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmBh, int M, int N, int K, int nfull,
-                   int num_tiles, EpiArgs ep) {
-  using C = GemmCfg<BN>;
+                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmX, int M,
+                   int N, int K, int nfull, int num_tiles, EpiArgs ep) {
+  using C = GemmCfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kEpiOff + C::kEpiBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* xbar = tempty + 2;  // [4][kXBufs] EPI_RESID: x chunk landed, per warp and buffer
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4 * C::kXBufs);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -298,6 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 8);  // 4 epilogue warps x 2 CTAs
     }
+    for (int i = 0; i < 4 * C::kXBufs; ++i) mbar_init(&xbar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -305,6 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (nfull < num_tiles) tma_prefetch_desc(&tmBh);
+    if (EPI == EPI_RESID) tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
     tmem_alloc_pair(tslot, C::kTmemCols);
@@ -387,18 +400,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int it = 0;
-    for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
+    int xu = 0;  // EPI_RESID: x chunks this warp has used (buffer xu & 1)
+    bool eok = true;
+    for (int t = cluster; t < num_tiles && eok; t += nclusters, ++it) {
       const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      gemm_epilogue<BN, EPI, F8>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
+      if constexpr (EPI == EPI_RESID) {
+        // x += tanh(g) acc for this warp's 32 rows, 32 columns at a time:
+        // TMA loads the x chunk (128-byte swizzled rows) into one of two
+        // buffers, each thread updates its row there, TMA stores it back
+        constexpr int NB = C::kXBufs;
+        uint8_t* eb = smem + C::kEpiOff + q * NB * 4096;
+        uint64_t* xb = xbar + NB * q;
+        const int row0 = (2 * ti.mp + rank) * kBM + q * 32;
+        const int row = row0 + lane;
+        const float sa = (F8 && row < M) ? ep.sa[row] : 1.f;
+        const int nch = ti.bn / 32;
+        auto load = [&](int c) {
+          if (lane == 0) {
+            const int b = (xu + c) % NB;
+            bulk_wait_read_all();  // the store that used buffer b last has read it
+            mbar_arrive_expect_tx(&xb[b], 4096);
+            tma_load_2d(eb + b * 4096, &tmX, &xb[b], ti.n0 + 32 * c, row0);
+          }
+        };
+        for (int c = 0; c < NB - 1 && c < nch; ++c) load(c);
+        for (int c = 0; c < nch; ++c) {
+          if (c + NB - 1 < nch) load(c + NB - 1);
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int u = xu + c;
+          const bool got =
+              mbar_wait(&xb[u % NB], static_cast<uint32_t>(u / NB) & 1u, abort_flag, &s_gemm_status);
+          tmem_ld_wait(r);
+          if (!got) {
+            eok = false;
+            break;
+          }
+          f8_scale<F8>(r, sa, ep.sw, ti.n0 + 32 * c);
+          float4* xs = reinterpret_cast<float4*>(eb + (u % NB) * 4096 + lane * 128);
+          const float4* g4 = reinterpret_cast<const float4*>(ep.gate + ti.n0 + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int pj = j ^ (lane & 7);  // 16-byte chunk j of row `lane` under the 128-byte swizzle
+            float4 v = xs[pj];
+            const float4 gv = __ldg(g4 + j);
+            v.x = fmaf(gv.x, __uint_as_float(r[4 * j + 0]), v.x);
+            v.y = fmaf(gv.y, __uint_as_float(r[4 * j + 1]), v.y);
+            v.z = fmaf(gv.z, __uint_as_float(r[4 * j + 2]), v.z);
+            v.w = fmaf(gv.w, __uint_as_float(r[4 * j + 3]), v.w);
+            xs[pj] = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmX, eb + (u % NB) * 4096, ti.n0 + 32 * c, row0);
+            bulk_commit_group();
+          }
+        }
+        xu += nch;
+      } else {
+        gemm_epilogue<BN, EPI, F8>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_rank(&tempty[acc], 0));
     }
+    // the x stores of this warp have completed before the CTA leaves
+    if (EPI == EPI_RESID && lane == 0) bulk_wait_all();
   }
   // the partner may still be signalling this CTA's barriers: leave together
   __syncwarp();
@@ -429,18 +502,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // inner x outer.
 static cudaError_t encode_f16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
                                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                                 bool bytes = false) {
+                                 bool bytes = false, bool f32 = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+  const CUresult r = fn(m,
+                        f32     ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                        : bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2,
                         const_cast<void*>(ptr), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// EPI_RESID: the f32 residual x [M][ldo] in 32 x 32 boxes (128-byte
+// swizzled rows); other epilogues carry an unused copy of the A map.
+static cudaError_t encode_x_map(GemmPlan* p) {
+  if (p->epi != EPI_RESID) {
+    p->tmX = p->tmA;
+    return cudaSuccess;
+  }
+  return encode_f16_2d(&p->tmX, p->out, p->N, p->M, static_cast<uint64_t>(p->ldo) * 4, 32, 32, false, true);
 }
 
 cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
@@ -462,7 +549,9 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   // split tail)
   e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2);
   if (e != cudaSuccess) return e;
-  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4);
+  e = encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4);
+  if (e != cudaSuccess) return e;
+  return encode_x_map(p);
 }
 
 cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const uint8_t* A, const float* sa,
@@ -483,12 +572,14 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
   if (e != cudaSuccess) return e;
   e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 2, true);
   if (e != cudaSuccess) return e;
-  return encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, true);
+  e = encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, true);
+  if (e != cudaSuccess) return e;
+  return encode_x_map(p);
 }
 
 template <int BN, int EPI, bool F8 = false>
 static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI>;
   static int max_clusters = 0;
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>,
@@ -514,8 +605,8 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   }
   const int clusters = std::min(total, max_clusters);
   EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw};
-  gemm_tc_kernel<BN, EPI, F8><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.M, p.N, p.K, nfull,
-                                                                   total, ep);
+  gemm_tc_kernel<BN, EPI, F8><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.tmX, p.M, p.N, p.K,
+                                                                   nfull, total, ep);
   return cudaGetLastError();
 }
 
