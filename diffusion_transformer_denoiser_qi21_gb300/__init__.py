@@ -19,7 +19,7 @@ __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
     "timestep_mods", "denoise", "set_checks", "PackedLayerFp8", "pack_layer_fp8", "workspace_bytes_fp8",
-    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
+    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -221,6 +221,20 @@ def graph_step_batch(g: Geom, layers, caches, x_in, x_out, mods, workspace) -> G
                                        _ptr(workspace, None, "workspace"),
                                        workspace.numel() * workspace.element_size(), C.byref(h)))
     return Graph(h, (layers, caches, x_in, x_out, mods, workspace, lay))
+
+
+def graph_step_batch_fp8(g: Geom, layers8, caches, x_in, x_out, mods, workspace) -> Graph:
+    """qi21_graph_step_batch_fp8: record one FP8 step of every cache's sequence."""
+    torch = _torch()
+    f = torch.float32
+    arr = (C.c_void_p * len(caches))(*[c.handle.value for c in caches])
+    h = C.c_void_p()
+    lay = _layer8_array(layers8)
+    check(load().qi21_graph_step_batch_fp8(C.byref(g), lay, arr, len(caches), _ptr(x_in, f, "x_in"),
+                                           _ptr(x_out, f, "x_out"), _ptr(mods, f, "mods"),
+                                           _ptr(workspace, None, "workspace"),
+                                           workspace.numel() * workspace.element_size(), C.byref(h)))
+    return Graph(h, (layers8, caches, x_in, x_out, mods, workspace, lay))
 
 
 def graph_denoise_batch(g: Geom, layers, caches, tok, w_in, mods, final_scale, w_out, out, workspace) -> Graph:

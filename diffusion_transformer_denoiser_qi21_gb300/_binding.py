@@ -92,6 +92,7 @@ _SIGS = {
     "qi21_graph_step_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, C.c_size_t, C.POINTER(_vp)]),
     "qi21_graph_denoise_batch": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t,
                                            C.POINTER(_vp)]),
+    "qi21_graph_step_batch_fp8": (C.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, C.c_size_t, C.POINTER(_vp)]),
     "qi21_graph_launch": (C.c_int, [_vp, _vp]),
     "qi21_graph_free": (None, [_vp]),
     "qi21_count_nonfinite": (C.c_int, [_vp, C.c_size_t, _i32, C.POINTER(C.c_uint64), _vp]),

@@ -1062,6 +1062,16 @@ int qi21_graph_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi
       out);
 }
 
+int qi21_graph_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, const qi21_kvcache* const* caches,
+                              int32_t nseq, const float* x_in, float* x_out, const float* mods, void* workspace,
+                              size_t ws_bytes, qi21_graph** out) {
+  return capture_graph(
+      [&](void* cs) {
+        return qi21_step_batch_fp8(g, layers, caches, nseq, x_in, x_out, mods, nullptr, workspace, ws_bytes, cs);
+      },
+      out);
+}
+
 int qi21_graph_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches,
                              int32_t nseq, const float* tok, const float* w_in, const float* mods,
                              const float* final_scale, const float* w_out, float* out_v, void* workspace,

@@ -396,6 +396,13 @@ int qi21_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers,
                         float* x_out, const float* mods, float* x_layers, void* workspace,
                         size_t ws_bytes, void* stream);
 
+/* The FP8 step recorded as a graph, as qi21_graph_step_batch (replay with
+ * qi21_graph_launch, release with qi21_graph_free). */
+int qi21_graph_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers,
+                              const qi21_kvcache* const* caches, int32_t nseq, const float* x_in,
+                              float* x_out, const float* mods, void* workspace, size_t ws_bytes,
+                              qi21_graph** out);
+
 /* Reads and clears the device status word (0 = fine; nonzero = a kernel
  * gave up waiting). Synchronises the device. */
 int qi21_device_status(void);

@@ -106,3 +106,20 @@ def test_graph_capture_refuses_what_the_call_refuses():
     gr.launch()
     ref = _direct_step(dw, dw.x_target, dw.mods_t)
     np.testing.assert_array_equal(host(dw.x_out), ref)
+
+
+def test_graph_fp8_step_equals_direct():
+    w = S.WORKLOADS["cfg_pair_d256"]
+    dw = D.DeviceWorkload(w)
+    l8 = [q.pack_layer_fp8(dw.g, l) for l in dw.layers]
+    rows = max(w.nseq * w.n_target, max(c.lp for c in dw.caches))
+    ws = torch.empty(q.workspace_bytes_fp8(dw.g, rows), dtype=torch.uint8, device="cuda")
+    for s, c in enumerate(dw.caches):
+        q.prefill_fp8(dw.g, l8, c, dw.x_prefix[s], dw.mods0, ws)
+    x_out = torch.empty_like(dw.x_target)
+    gr = q.graph_step_batch_fp8(dw.g, l8, dw.caches, dw.x_target, x_out, dw.mods_t, ws)
+    ref = torch.empty_like(x_out)
+    q.step_batch_fp8(dw.g, l8, dw.caches, dw.x_target, ref, dw.mods_t, ws)
+    gr.launch()
+    np.testing.assert_array_equal(host(x_out), host(ref))
+    gr.free()
