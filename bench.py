@@ -87,8 +87,12 @@ def class_work(w, n_rows, vis_sum):
 NCU_TRAFFIC = {
     "attention": ("k_attn.cu", "31e2c2f8ce3fc70b353bdbeae0edc7a3ab41c6cf149584d9d5ab604720533dd2",
                   168198400 + 20426880),
-    "gateup": ("k_gemm.cu", "7a532772def56fdd53aebf3366366c284d84f1360d65f94d35884df375714ad2",
-               249069568 + 87047808),
+    "gateup": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
+               (245545728 + 245613312) // 2 + (86691328 + 86847744) // 2),
+    "o": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
+          (153350400 + 151731456) // 2 + (33058048 + 33457408) // 2),
+    "down": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
+             (587918080 + 588015360) // 2 + (59550976 + 59887360) // 2),
 }
 
 
