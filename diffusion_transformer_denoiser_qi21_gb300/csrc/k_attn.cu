@@ -9,24 +9,29 @@
 //
 // CTA = one 128-query tile of one head of one sequence, 10 warps:
 //   warp 0     TMA: Q once (2 x 64-column boxes, 128-byte swizzle), then K
-//              and V blocks of 128 keys into a 2-stage ring. The cache part
-//              of the key axis is padded to a multiple of 128 so no block
+//              and V blocks of 192 keys into 2-stage rings. The cache part
+//              of the key axis is padded to a multiple of 192 so no block
 //              straddles the two sources (padding keys are masked).
 //   warp 1     TMEM allocation and the single MMA-issuing thread:
-//              S_j = Q K_j^T into one of two TMEM buffers (kind::f16, f32
-//              accumulate), then O += P_j V_j with P read from TMEM and V an
-//              MN-major shared-memory operand.
-//   warps 2-9  softmax: two warps per TMEM lane quadrant, each owning 64 of
-//              the 128 key columns of its 32 query rows. Per block: read S_j
+//              S_j = Q K_j^T (M 128, N 192) into one of two TMEM buffers
+//              (kind::f16, f32 accumulate), then O += P_j V_j (12 MMAs of
+//              K 16) with P read from TMEM and V an MN-major shared-memory
+//              operand.
+//   warps 2-9  softmax: two warps per TMEM lane quadrant, each owning 96 of
+//              the 192 key columns of its 32 query rows. Per block: read S_j
 //              with tcgen05.ld, mask, exchange the partial row max with the
-//              partner warp (shared memory + a 64-thread named barrier), keep
-//              a running max that is only raised when a block exceeds it by
-//              more than 2^8 (then O is rescaled in TMEM), write
-//              P_j = 2^(s - m) as packed f16 pairs into TMEM (the A operand
-//              of P V, one of two P buffers) and accumulate the row sum; at
-//              the end O / l -> f16 rows of the output.
-// The QK^T of block j+1 and the P V of block j-1 run on the tensor cores
-// while the softmax of block j runs on the ALUs. Every wait is bounded.
+//              partner warp (a bounded mbarrier rendezvous), keep a running
+//              max that is only raised when a block exceeds it by more than
+//              2^8 (then O is rescaled in TMEM), write P_j = 2^(s - m) as
+//              packed f16 pairs over the first 96 columns of S_j's buffer
+//              (the A operand of P V; both warps of the quadrant have read
+//              their S by then) and accumulate the row sum; at the end
+//              O / l -> f16 rows of the output.
+// TMEM: S buffers [0, 192), [192, 384), O [384, 512). The QK^T of block
+// j+1 and the P V of block j-1 run on the tensor cores while the softmax of
+// block j runs on the ALUs; 192-key blocks (against 128) spread each
+// block's fixed handshake cost over 1.5x the MMA work. Every wait is
+// bounded.
 #include <algorithm>
 #include <cstdio>
 
@@ -47,27 +52,30 @@ unsigned int attn_status_read_clear() {
 }
 
 constexpr int kAQ = 128;              // queries per CTA
-constexpr int kAK = 128;              // keys per block
+constexpr int kAK = 192;              // keys per block
 constexpr int kAD = 128;              // head dim
-constexpr int kSub = 128 * 64 * 2;    // one 128-row x 64-column f16 swizzled box: 16 KB
-constexpr int kTileBytes = 2 * kSub;  // 128 x 128 f16
+constexpr int kSub = 128 * 64 * 2;    // one 128-row x 64-column f16 swizzled box: 16 KB (Q)
+constexpr int kTileBytes = 2 * kSub;  // Q: 128 x 128 f16
+constexpr int kKVSub = kAK * 64 * 2;  // one 192-row x 64-column box: 24 KB (K, V)
+constexpr int kKVBytes = 2 * kKVSub;  // a K or V block: 192 x 128 f16
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;      // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kOffK = kOffQ + kTileBytes;    // 2 stages
+constexpr int kOffV = kOffK + 2 * kKVBytes;  // 2 stages
+constexpr int kOffBar = kOffV + 2 * kKVBytes;
 constexpr int kOffX = kOffBar + 256;        // partial row max / sum exchange [2][128] f32
 constexpr int kAttnSmem = kOffX + 1024 + 1024;
 constexpr int kAttnThreads = 320;           // 10 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 in f16
 
 struct AttnTcSeq {
-  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 128 (unused if n_pre == 0)
+  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 192 (unused if n_pre == 0)
   const uint32_t* vis;
   int n_pre, pad_end, q_row0, nq, own_row0, n_own;
 };
 
 struct AttnTcParams {
-  CUtensorMap panel;  // [rows][3H] f16, box 64 x 128
+  CUtensorMap panel;     // [rows][3H] f16, box 64 x 128 (Q)
+  CUtensorMap panel_kv;  // same, box 64 x 192 (K, V)
   __half* out;
   int H;
   float scale_log2;
@@ -111,6 +119,15 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 columns of 32-bit stored from registers to this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
 }
 
 // key index of virtual key v (cache keys, padding, then own keys), or a
@@ -160,6 +177,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.panel);
+    tma_prefetch_desc(&p.panel_kv);
     if (sq.n_pre > 0) tma_prefetch_desc(&sq.kvmap);
   }
   if (warp == 1) {
@@ -170,9 +188,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS = tmem;         // S buffers at columns [0, 256)
-  const uint32_t tO = tmem + 256;   // O at columns [256, 384)
-  const uint32_t tP = tmem + 384;   // P buffers (f16 pairs) at [384, 448), [448, 512)
+  const uint32_t tS = tmem;         // S buffers at columns [0, 192), [192, 384)
+  const uint32_t tO = tmem + 384;   // O at columns [384, 512)
+  // P_b (f16 pairs, 96 columns) over the first columns of S_b: written only
+  // after both warps of a quadrant have read their S (the row-max exchange)
+  const uint32_t tP = tS;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -184,32 +204,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       auto load_k = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(&kempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
-        uint8_t* kd = smem + kOffK + st * kTileBytes;
+        uint8_t* kd = smem + kOffK + st * kKVBytes;
         const int v0 = j * kAK;
-        mbar_arrive_expect_tx(&kfull[st], kTileBytes);
+        mbar_arrive_expect_tx(&kfull[st], kKVBytes);
         if (v0 < sq.n_pre) {
           tma_load_2d(kd, &sq.kvmap, &kfull[st], h * kAD, v0);
-          tma_load_2d(kd + kSub, &sq.kvmap, &kfull[st], h * kAD + 64, v0);
+          tma_load_2d(kd + kKVSub, &sq.kvmap, &kfull[st], h * kAD + 64, v0);
         } else {
           const int row = sq.own_row0 + (v0 - sq.pad_end);
-          tma_load_2d(kd, &p.panel, &kfull[st], H + h * kAD, row);
-          tma_load_2d(kd + kSub, &p.panel, &kfull[st], H + h * kAD + 64, row);
+          tma_load_2d(kd, &p.panel_kv, &kfull[st], H + h * kAD, row);
+          tma_load_2d(kd + kKVSub, &p.panel_kv, &kfull[st], H + h * kAD + 64, row);
         }
         return true;
       };
       auto load_v = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(&vempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
-        uint8_t* vd = smem + kOffV + st * kTileBytes;
+        uint8_t* vd = smem + kOffV + st * kKVBytes;
         const int v0 = j * kAK;
-        mbar_arrive_expect_tx(&vfull[st], kTileBytes);
+        mbar_arrive_expect_tx(&vfull[st], kKVBytes);
         if (v0 < sq.n_pre) {
           tma_load_2d(vd, &sq.kvmap, &vfull[st], H + h * kAD, v0);
-          tma_load_2d(vd + kSub, &sq.kvmap, &vfull[st], H + h * kAD + 64, v0);
+          tma_load_2d(vd + kKVSub, &sq.kvmap, &vfull[st], H + h * kAD + 64, v0);
         } else {
           const int row = sq.own_row0 + (v0 - sq.pad_end);
-          tma_load_2d(vd, &p.panel, &vfull[st], 2 * H + h * kAD, row);
-          tma_load_2d(vd + kSub, &p.panel, &vfull[st], 2 * H + h * kAD + 64, row);
+          tma_load_2d(vd, &p.panel_kv, &vfull[st], 2 * H + h * kAD, row);
+          tma_load_2d(vd + kKVSub, &p.panel_kv, &vfull[st], 2 * H + h * kAD + 64, row);
         }
         return true;
       };
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
+      constexpr uint32_t idesc_qk = idesc_f16(128, kAK, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, 128, true);  // V: MN-major
       const uint32_t sQ = smem_u32(smem + kOffQ);
       bool ok = mbar_wait(qfull, 0, abort_flag, &s_attn_status);
@@ -229,13 +249,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
         const int s = j & 1;
         if (!mbar_wait(&kfull[s], (j >> 1) & 1, abort_flag, &s_attn_status)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(smem + kOffK + s * kTileBytes);
+        const uint32_t sK = smem_u32(smem + kOffK + s * kKVBytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * kSub;
-          tc_mma_f16(tS + (j & 1) * 128, sdesc_sw128(sQ + off) + 2 * (k & 3),
-                     sdesc_sw128(sK + off) + 2 * (k & 3), idesc_qk, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)
+          tc_mma_f16(tS + (j & 1) * kAK, sdesc_sw128(sQ + (k >> 2) * kSub) + 2 * (k & 3),
+                     sdesc_sw128(sK + (k >> 2) * kKVSub) + 2 * (k & 3), idesc_qk, k > 0 ? 1u : 0u);
         tc_commit(&kempty[s]);
         tc_commit(&sfull[j & 1]);
         return true;
@@ -248,14 +266,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
         const int s = j & 1;
         if (!mbar_wait(&vfull[s], (j >> 1) & 1, abort_flag, &s_attn_status)) break;
         tc_fence_after();
-        const uint32_t sV = smem_u32(smem + kOffV + s * kTileBytes);
+        const uint32_t sV = smem_u32(smem + kOffV + s * kKVBytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kAK / 16; ++k) {
           // A = P in TMEM: 128 query lanes x 16 keys = 8 columns of f16
           // pairs; B = V: 16 key rows x 128 d, d contiguous (two 64-wide
-          // atoms kSub apart, 8-row groups 1 KB)
-          const uint64_t b = sdesc(sV + k * 2048, kSub, 1024, 2);
-          tc_mma_f16_ts(tO, tP + pb * 64 + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          // atoms kKVSub apart, 8-row groups 1 KB)
+          const uint64_t b = sdesc(sV + k * 2048, kKVSub, 1024, 2);
+          tc_mma_f16_ts(tO, tP + pb * kAK + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&vempty[s]);
         tc_commit(&pvdone[pb]);
@@ -291,37 +309,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      uint32_t s[2][32];
-      tmem_ld32(tS + b * 128 + lane_off + hf * 64, s[0]);
-      tmem_ld32(tS + b * 128 + lane_off + hf * 64 + 32, s[1]);
-      tmem_ld_wait(s[0]);
-      tmem_ld_wait(s[1]);
-      const int v0 = j * kAK + hf * 64;
+      constexpr int kHalf = kAK / 2;  // 96 key columns per warp
+      uint32_t s[3][32];
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) tmem_ld32(tS + b * kAK + lane_off + hf * kHalf + cc * 32, s[cc]);
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) tmem_ld_wait(s[cc]);
+      const int v0 = j * kAK + hf * kHalf;
       // every key of this half-block visible to this row?
       const int k0 = key_index(v0, sq.n_pre, sq.pad_end);
-      const int k1 = key_index(v0 + 63, sq.n_pre, sq.pad_end);
-      const bool same_src = (v0 + 64 <= sq.n_pre) || (v0 >= sq.pad_end);
+      const int k1 = key_index(v0 + kHalf - 1, sq.n_pre, sq.pad_end);
+      const bool same_src = (v0 + kHalf <= sq.n_pre) || (v0 >= sq.pad_end);
       if (!(same_src && k1 < lim && k0 < lim)) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int cc = 0; cc < 3; ++cc)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int kj = key_index(v0 + cc * 32 + e, sq.n_pre, sq.pad_end);
             if (kj >= lim) s[cc][e] = __float_as_uint(-INFINITY);
           }
       }
-      float mx[4];
+      float mx[6];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) mx[a] = __uint_as_float(s[a >> 1][(a & 1) * 16]);
+      for (int a = 0; a < 6; ++a) mx[a] = __uint_as_float(s[a >> 1][(a & 1) * 16]);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 6; ++a)
 #pragma unroll
         for (int e = 1; e < 15; e += 2)
           mx[a] = max3(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + e]),
                        __uint_as_float(s[a >> 1][(a & 1) * 16 + e + 1]));
 #pragma unroll
-      for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + 15]));
-      const float pmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      for (int a = 0; a < 6; ++a) mx[a] = fmaxf(mx[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + 15]));
+      const float pmax = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), mx[0]);
       // the partner warp holds the other 64 columns of these rows
       xch[hf * 128 + r] = pmax;
       if (!pair_sync()) {
@@ -351,22 +370,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
           break;
         }
       }
-      // this half of the P row -> TMEM: 64 keys = 32 columns of f16 pairs
+      // this half of the P row -> TMEM: 96 keys = 48 columns of f16 pairs
+      // (32 + 16) over S_b
       const uint64_t nm2 = f2(-m, -m);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int k = 2 * i;
-        const uint64_t x = ffma2(f2(__uint_as_float(s[k >> 5][k & 31]), __uint_as_float(s[k >> 5][(k & 31) + 1])),
-                                 c2, nm2);
-        float x0, x1;
-        unf2(x, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        acc[i & 3] = fadd2(acc[i & 3], f2(p0, p1));
-        pk[i] = pack_half2(p0, p1);
+      for (int part = 0; part < 2; ++part) {
+        uint32_t pk[32];
+        const int npairs = part == 0 ? 32 : 16;
+#pragma unroll
+        for (int i = 0; i < npairs; ++i) {
+          const int k = 2 * (32 * part + i);
+          const uint64_t x =
+              ffma2(f2(__uint_as_float(s[k >> 5][k & 31]), __uint_as_float(s[k >> 5][(k & 31) + 1])), c2, nm2);
+          float x0, x1;
+          unf2(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc[i & 3] = fadd2(acc[i & 3], f2(p0, p1));
+          pk[i] = pack_half2(p0, p1);
+        }
+        if (part == 0)
+          tmem_st32(tP + b * kAK + hf * (kHalf / 2) + lane_off, pk);
+        else
+          tmem_st16(tP + b * kAK + hf * (kHalf / 2) + 32 + lane_off, pk);
       }
-      tmem_st32(tP + b * 64 + hf * 32 + lane_off, pk);
       {
         const uint64_t t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
         float t0, t1;
@@ -442,12 +469,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
   return fn;
 }
 
-static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
   auto fn = attn_encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -469,7 +496,8 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
   prm.out = in.out;
   prm.H = H;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kAD)));
-  cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows);
+  cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAQ);
+  if (e == cudaSuccess) e = encode_rows(&prm.panel_kv, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAK);
   if (e != cudaSuccess) return e;
   int maxq = 0;
   for (int i = 0; i < in.nseq; ++i) {
@@ -483,7 +511,7 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
     t.own_row0 = a.own_row0;
     t.n_own = a.n_own;
     if (a.n_pre > 0) {
-      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre);
+      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre, kAK);
       if (e != cudaSuccess) return e;
     }
     maxq = std::max(maxq, a.nq);
