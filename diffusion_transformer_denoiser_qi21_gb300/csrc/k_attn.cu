@@ -9,9 +9,11 @@
 //
 // CTA = one 128-query tile of one head of one sequence, 10 warps:
 //   warp 0     TMA: Q once (2 x 64-column boxes, 128-byte swizzle), then K
-//              and V blocks of 192 keys into 2-stage rings. The cache part
-//              of the key axis is padded to a multiple of 192 so no block
-//              straddles the two sources (padding keys are masked).
+//              and V blocks of 192 keys into 2-stage rings, each block as
+//              three 64-key boxes. The cache part of the key axis is padded
+//              to a multiple of 64 so no box straddles the two sources
+//              (padding keys are masked); a block may hold cache and panel
+//              boxes, so at most 63 padding keys are computed per query.
 //   warp 1     TMEM allocation and the single MMA-issuing thread:
 //              S_j = Q K_j^T (M 128, N 192) into one of two TMEM buffers
 //              (kind::f16, f32 accumulate), then O += P_j V_j (12 MMAs of
@@ -56,7 +58,8 @@ constexpr int kAK = 192;              // keys per block
 constexpr int kAD = 128;              // head dim
 constexpr int kSub = 128 * 64 * 2;    // one 128-row x 64-column f16 swizzled box: 16 KB (Q)
 constexpr int kTileBytes = 2 * kSub;  // Q: 128 x 128 f16
-constexpr int kKVSub = kAK * 64 * 2;  // one 192-row x 64-column box: 24 KB (K, V)
+constexpr int kKVSub = kAK * 64 * 2;  // 192 rows x 64 columns of a K or V block: 24 KB
+constexpr int kKVBox = 64;            // rows per K / V box (the padding unit of the cache keys)
 constexpr int kKVBytes = 2 * kKVSub;  // a K or V block: 192 x 128 f16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;    // 2 stages
@@ -68,14 +71,14 @@ constexpr int kAttnThreads = 320;           // 10 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 in f16
 
 struct AttnTcSeq {
-  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 192 (unused if n_pre == 0)
+  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 64 (unused if n_pre == 0)
   const uint32_t* vis;
   int n_pre, pad_end, q_row0, nq, own_row0, n_own;
 };
 
 struct AttnTcParams {
   CUtensorMap panel;     // [rows][3H] f16, box 64 x 128 (Q)
-  CUtensorMap panel_kv;  // same, box 64 x 192 (K, V)
+  CUtensorMap panel_kv;  // same, box 64 x 64 (K, V)
   __half* out;
   int H;
   float scale_log2;
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   const int q_last = min(qt0 + kAQ, sq.nq) - 1;
   const int lim_last = sq.vis ? min(ntot, static_cast<int>(__ldg(sq.vis + q_last))) : ntot;
   const int own_need = max(0, lim_last - sq.n_pre);
-  const int nkb = sq.pad_end / kAK + (own_need + kAK - 1) / kAK;
+  const int nkb = (sq.pad_end + own_need + kAK - 1) / kAK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 15; ++i) mbar_init(&bars[i], (i == 11 || i == 12) ? 256 : 1);
@@ -201,36 +204,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       tma_load_2d(smem + kOffQ, &p.panel, qfull, h * kAD, qy);
       tma_load_2d(smem + kOffQ + kSub, &p.panel, qfull, h * kAD + 64, qy);
       // need order: K_{j+1} (for QK^T one block ahead), then V_j (for P V)
+      // a K or V block = three 64-key boxes, each wholly from the cache
+      // (keys padded to a multiple of 64) or wholly from the panel
+      auto load_kv = [&](uint8_t* dst, uint64_t* bar, int j, int col_cache, int col_panel) {
+#pragma unroll
+        for (int sb = 0; sb < kAK / kKVBox; ++sb) {
+          const int v = j * kAK + sb * kKVBox;
+          uint8_t* d = dst + sb * kKVBox * 128;
+          if (v < sq.n_pre) {
+            tma_load_2d(d, &sq.kvmap, bar, col_cache, v);
+            tma_load_2d(d + kKVSub, &sq.kvmap, bar, col_cache + 64, v);
+          } else {
+            const int row = sq.own_row0 + (v - sq.pad_end);
+            tma_load_2d(d, &p.panel_kv, bar, col_panel, row);
+            tma_load_2d(d + kKVSub, &p.panel_kv, bar, col_panel + 64, row);
+          }
+        }
+      };
       auto load_k = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(&kempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
-        uint8_t* kd = smem + kOffK + st * kKVBytes;
-        const int v0 = j * kAK;
         mbar_arrive_expect_tx(&kfull[st], kKVBytes);
-        if (v0 < sq.n_pre) {
-          tma_load_2d(kd, &sq.kvmap, &kfull[st], h * kAD, v0);
-          tma_load_2d(kd + kKVSub, &sq.kvmap, &kfull[st], h * kAD + 64, v0);
-        } else {
-          const int row = sq.own_row0 + (v0 - sq.pad_end);
-          tma_load_2d(kd, &p.panel_kv, &kfull[st], H + h * kAD, row);
-          tma_load_2d(kd + kKVSub, &p.panel_kv, &kfull[st], H + h * kAD + 64, row);
-        }
+        load_kv(smem + kOffK + st * kKVBytes, &kfull[st], j, h * kAD, H + h * kAD);
         return true;
       };
       auto load_v = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(&vempty[st], ((j >> 1) & 1) ^ 1u, abort_flag, &s_attn_status)) return false;
-        uint8_t* vd = smem + kOffV + st * kKVBytes;
-        const int v0 = j * kAK;
         mbar_arrive_expect_tx(&vfull[st], kKVBytes);
-        if (v0 < sq.n_pre) {
-          tma_load_2d(vd, &sq.kvmap, &vfull[st], H + h * kAD, v0);
-          tma_load_2d(vd + kKVSub, &sq.kvmap, &vfull[st], H + h * kAD + 64, v0);
-        } else {
-          const int row = sq.own_row0 + (v0 - sq.pad_end);
-          tma_load_2d(vd, &p.panel_kv, &vfull[st], 2 * H + h * kAD, row);
-          tma_load_2d(vd + kKVSub, &p.panel_kv, &vfull[st], 2 * H + h * kAD + 64, row);
-        }
+        load_kv(smem + kOffV + st * kKVBytes, &vfull[st], j, H + h * kAD, 2 * H + h * kAD);
         return true;
       };
       bool ok = load_k(0);
@@ -497,7 +499,7 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
   prm.H = H;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kAD)));
   cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAQ);
-  if (e == cudaSuccess) e = encode_rows(&prm.panel_kv, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAK);
+  if (e == cudaSuccess) e = encode_rows(&prm.panel_kv, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kKVBox);
   if (e != cudaSuccess) return e;
   int maxq = 0;
   for (int i = 0; i < in.nseq; ++i) {
@@ -505,13 +507,13 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
     AttnTcSeq& t = prm.seq[i];
     t.vis = a.vis;
     t.n_pre = a.n_pre;
-    t.pad_end = (a.n_pre + kAK - 1) / kAK * kAK;
+    t.pad_end = (a.n_pre + kKVBox - 1) / kKVBox * kKVBox;
     t.q_row0 = a.q_row0;
     t.nq = a.nq;
     t.own_row0 = a.own_row0;
     t.n_own = a.n_own;
     if (a.n_pre > 0) {
-      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre, kAK);
+      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre, kKVBox);
       if (e != cudaSuccess) return e;
     }
     maxq = std::max(maxq, a.nq);

@@ -222,6 +222,10 @@ def _attn_case(case, heads, nq, n_own, n_pre, vis=None):
     (2, 64, 64, 4114),      # a long cache, block boundary inside the cache
     (4, 200, 200, 63),      # prefix/panel boundary one short of a key block
     (32, 129, 129, 1),
+    (2, 100, 100, 64),      # cache of exactly one 64-key box: a block of cache and panel boxes
+    (2, 5, 5, 70),          # padded cache boxes, then a panel box reaching past the panel
+    (3, 300, 300, 191),
+    (2, 140, 140, 129),
 ])
 def test_attention_step_mode(heads, nq, n_own, n_pre):
     got, ref = _attn_case(nq * 31 + n_pre, heads, nq, n_own, n_pre)
