@@ -459,15 +459,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 // ---------------------------------------------------------------- host ----
 
 static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  // resolved once, thread-safely, on first use
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult qr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &qr) == cudaSuccess &&
         qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -485,13 +486,9 @@ static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, u
 }
 
 cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAttnSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  if (attr != cudaSuccess) return attr;
   AttnTcParams prm;
   memset(&prm, 0, sizeof prm);
   const int H = in.heads * kAD;

@@ -486,15 +486,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 // ---------------------------------------------------------------- host ----
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  // resolved once, thread-safely, on first use
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -580,20 +581,28 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
 template <int BN, int EPI, bool F8 = false>
 static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   using C = GemmCfg<BN, EPI>;
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
+  // shared-memory opt-in and the resident cluster count, once per
+  // instance, thread-safely, on first use
+  struct Init {
+    cudaError_t e;
+    int clusters;
+  };
+  static const Init init = [] {
+    Init r{cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmem),
+           1};
+    if (r.e != cudaSuccess) return r;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * sm_count(), 1, 1);
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, F8>, &cfg);
-    if (e != cudaSuccess) return e;
-    max_clusters = n > 0 ? n : 1;
-  }
+    r.e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, F8>, &cfg);
+    r.clusters = n > 0 ? n : 1;
+    return r;
+  }();
+  if (init.e != cudaSuccess) return init.e;
+  const int max_clusters = init.clusters;
   const int num_mp = ((p.M + kBM - 1) / kBM + 1) / 2;
   const int pairs = num_mp * (p.N / BN);
   // split the pairs of a partial last wave that is at most half full
