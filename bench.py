@@ -85,14 +85,14 @@ def class_work(w, n_rows, vis_sum):
 # (profiles/dram_traffic_step32_cond4114_n4096.md). Reported only while the
 # source is unchanged.
 NCU_TRAFFIC = {
-    "attention": ("k_attn.cu", "cfcd80c37e8f39da3444a118a585cabe6e98ca4ba985ec8ce990bd633214a029",
-                  (168180480 + 168261632) // 2 + (21294848 + 19254784) // 2),
-    "gateup": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
-               (245545728 + 245613312) // 2 + (86691328 + 86847744) // 2),
-    "o": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
-          (153350400 + 151731456) // 2 + (33058048 + 33457408) // 2),
-    "down": ("k_gemm.cu", "467f62e9def4aaa9863a57f22c9f4556c716e5fd733037772914ba19396f5e00",
-             (587918080 + 588015360) // 2 + (59550976 + 59887360) // 2),
+    "attention": ("k_attn.cu", "a2ffc7192710e63f6af1716b7e9949804dea9705a429680f5d27ea565cf17e83",
+                  (168189184 + 168228096) // 2 + (21861120 + 19226880) // 2),
+    "gateup": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
+               (252058880 + 253903360) // 2 + (87711232 + 87821312) // 2),
+    "o": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
+          (148278528 + 147124736) // 2 + (31460864 + 31491072) // 2),
+    "down": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
+             (587750912 + 587684864) // 2 + (59443456 + 59263232) // 2),
 }
 
 
