@@ -13,7 +13,13 @@ frequencies, f32 angle, f32 cos/sin). Matrix products use numpy's ``@``
 (a library primitive) with no blocking or reordering of the definition.
 
 Pinned by ``tests/test_oracle_pins.py`` (worked examples of the page's own
-tests, closed forms, brute force and invariants).
+tests, closed forms, brute force and invariants). Helpers without a pin of
+their own (``gated_add``, ``linear_row``) are pinned through the functions
+that use them (the zero-gate identity, the closed-form blocks, the
+timestep chain). The absolute values of a full-size block are parity
+unpinned: the pages print no activations, so they rest on the pinned
+pieces and on the invariants (prefill + step = joint forward under the
+block-causal mask; blocks with Wq = Wk = 0 or Wv = 0 in closed form).
 """
 from __future__ import annotations
 
