@@ -55,7 +55,9 @@ def test_mods_prep():
         np.testing.assert_allclose(host(md), O.mods_dev(m, dim), rtol=0, atol=2e-7)
 
 
-@pytest.mark.parametrize("rows,dim", [(1, 128), (130, 512), (37, 4096), (3, 8192), (0, 256)])
+# row counts above the resident CTA count make each CTA walk several rows
+@pytest.mark.parametrize("rows,dim", [(1, 128), (130, 512), (37, 4096), (3, 8192), (0, 256), (2000, 4096),
+                                      (700, 8192), (4099, 1024)])
 def test_rowop_norm(rows, dim):
     x = S.op_tensor(2, dim, 0, (rows, dim), 3.0, offset=0.5)
     sc = S.op_tensor(2, dim, 1, (dim,), 0.1)
@@ -70,7 +72,7 @@ def test_rowop_norm(rows, dim):
     np.testing.assert_array_equal(host(xd), x)  # x untouched without y
 
 
-@pytest.mark.parametrize("rows,dim", [(5, 256), (64, 4096)])
+@pytest.mark.parametrize("rows,dim", [(5, 256), (64, 4096), (1500, 4096)])
 def test_rowop_gate_and_norm(rows, dim):
     x = S.op_tensor(3, dim, 0, (rows, dim), 1.0)
     y = S.op_tensor(3, dim, 1, (rows, dim), 1.0)
