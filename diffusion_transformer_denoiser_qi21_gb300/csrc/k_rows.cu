@@ -29,8 +29,11 @@ cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t
 }
 
 // ---------------------------------------------------------------- rowop ----
-// One 256-thread CTA per row, the row held in registers (NV float4 per
-// thread, NV = dim / 1024 rounded up to a power of two, dim <= 8192):
+// 256-thread CTAs, four per SM (two at NV = 8), each taking rows
+// blockIdx.x + k gridDim.x
+// with the next row's x loaded while the current one is reduced; a row is
+// held in registers (NV float4 per thread, NV = dim / 1024 rounded up to a
+// power of two, dim <= 8192):
 //   if y:  x += gate_t * y            (qwen_image21.rs, Qi21Dit::gated_add)
 //   if xn: xn = f16(LN(x) (1 + scale)) (Qi21Dit::norm_mod; affine-free LN,
 //          biased variance, two passes over the registers in f32)
@@ -46,63 +49,82 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   return ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
 }
 
+// resident CTAs per SM: four, two for the widest rows (register budget)
+constexpr int rowop_ctas_per_sm(int nv) { return nv >= 8 ? 2 : 4; }
+
 template <int NV>
-__global__ void __launch_bounds__(kRowThreads) rowop_kernel(int dim, float eps, float* __restrict__ x,
-                                                            const float* __restrict__ y,
-                                                            const float* __restrict__ gate_t,
-                                                            const float* __restrict__ scale,
-                                                            __half* __restrict__ xn) {
+__global__ void __launch_bounds__(kRowThreads, rowop_ctas_per_sm(NV)) rowop_kernel(int rows, int dim, float eps, float* __restrict__ x,
+                                                               const float* __restrict__ y,
+                                                               const float* __restrict__ gate_t,
+                                                               const float* __restrict__ scale,
+                                                               __half* __restrict__ xn) {
   __shared__ float red[8];
-  const size_t row = blockIdx.x;
   const int nv = dim >> 2;
-  float4* x4 = reinterpret_cast<float4*>(x + row * dim);
-  float4 v[NV];
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int idx = threadIdx.x + j * kRowThreads;
-    if (idx < nv) v[j] = x4[idx];
-  }
-  if (y != nullptr) {
+  // rows blockIdx.x, + gridDim.x, ...: the next row's x is loaded while
+  // this row is reduced and written
+  float4 v[NV], nx[NV];
+  auto load_row = [&](int rw, float4 (&d)[NV]) {
+    const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(rw) * dim);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int idx = threadIdx.x + j * kRowThreads;
-      if (idx < nv) {
-        const float4 b = reinterpret_cast<const float4*>(y + row * dim)[idx];
-        const float4 g = reinterpret_cast<const float4*>(gate_t)[idx];
-        v[j].x = fmaf(g.x, b.x, v[j].x);
-        v[j].y = fmaf(g.y, b.y, v[j].y);
-        v[j].z = fmaf(g.z, b.z, v[j].z);
-        v[j].w = fmaf(g.w, b.w, v[j].w);
-        x4[idx] = v[j];
+      if (idx < nv) d[j] = src[idx];
+    }
+  };
+  int row = blockIdx.x;
+  if (row >= rows) return;
+  load_row(row, v);
+  while (true) {
+    const int next = row + static_cast<int>(gridDim.x);
+    if (next < rows) load_row(next, nx);
+    float4* x4 = reinterpret_cast<float4*>(x + static_cast<size_t>(row) * dim);
+    if (y != nullptr) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int idx = threadIdx.x + j * kRowThreads;
+        if (idx < nv) {
+          const float4 b = reinterpret_cast<const float4*>(y + static_cast<size_t>(row) * dim)[idx];
+          const float4 g = reinterpret_cast<const float4*>(gate_t)[idx];
+          v[j].x = fmaf(g.x, b.x, v[j].x);
+          v[j].y = fmaf(g.y, b.y, v[j].y);
+          v[j].z = fmaf(g.z, b.z, v[j].z);
+          v[j].w = fmaf(g.w, b.w, v[j].w);
+          x4[idx] = v[j];
+        }
       }
     }
-  }
-  if (xn == nullptr) return;
-  float sm = 0.f;
+    if (xn != nullptr) {
+      float sm = 0.f;
 #pragma unroll
-  for (int j = 0; j < NV; ++j)
-    if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-  const float mean = block_sum_256(sm, red) / static_cast<float>(dim);
-  float sq = 0.f;
+      for (int j = 0; j < NV; ++j)
+        if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+      const float mean = block_sum_256(sm, red) / static_cast<float>(dim);
+      float sq = 0.f;
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    if (threadIdx.x + j * kRowThreads < nv) {
-      const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
-      sq += (a * a + b * b) + (c * c + d * d);
+      for (int j = 0; j < NV; ++j) {
+        if (threadIdx.x + j * kRowThreads < nv) {
+          const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
+          sq += (a * a + b * b) + (c * c + d * d);
+        }
+      }
+      const float inv = rsqrtf(block_sum_256(sq, red) / static_cast<float>(dim) + eps);
+      uint2* o2 = reinterpret_cast<uint2*>(xn + static_cast<size_t>(row) * dim);
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int idx = threadIdx.x + j * kRowThreads;
+        if (idx < nv) {
+          const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
+          uint2 out;
+          out.x = pack_half2((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
+          out.y = pack_half2((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
+          o2[idx] = out;
+        }
+      }
     }
-  }
-  const float inv = rsqrtf(block_sum_256(sq, red) / static_cast<float>(dim) + eps);
-  uint2* o2 = reinterpret_cast<uint2*>(xn + row * dim);
+    if (next >= rows) break;
+    row = next;
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int idx = threadIdx.x + j * kRowThreads;
-    if (idx < nv) {
-      const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
-      uint2 out;
-      out.x = pack_half2((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
-      out.y = pack_half2((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
-      o2[idx] = out;
-    }
+    for (int j = 0; j < NV; ++j) v[j] = nx[j];
   }
 }
 
@@ -233,14 +255,16 @@ cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y,
                          const float* scale, __half* xn, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int per = (dim / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
+  // all CTAs resident, each walking rows with a stride of the grid
+  auto grid = [&](int nv) { return std::min(rows, rowop_ctas_per_sm(nv) * sm_count()); };
   if (per <= 1)
-    rowop_kernel<1><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<1><<<grid(1), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else if (per <= 2)
-    rowop_kernel<2><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<2><<<grid(2), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else if (per <= 4)
-    rowop_kernel<4><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<4><<<grid(4), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else
-    rowop_kernel<8><<<rows, kRowThreads, 0, s>>>(dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<8><<<grid(8), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   return cudaGetLastError();
 }
 
