@@ -45,6 +45,11 @@ static int cuda_fail(cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
+bool bind_primary_context() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
+}
+
 int sm_count() {
   // initialised once, thread-safely, on first use
   static const int n = [] {

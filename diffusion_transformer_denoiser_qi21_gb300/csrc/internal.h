@@ -121,6 +121,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 // --------------------------------------------------------------- device ----
 
 int sm_count();
+// Makes the current device's primary context current on a calling thread
+// that has none yet (what the first runtime call of a thread does), for
+// driver calls that need one (tensor-map encoding). True on success.
+bool bind_primary_context();
 // Sets the thread-local error text of qi21_last_error and returns code.
 int report_error(int code, const char* msg);
 // True while qi21_profile_enable(1) is in force (launches create events).
