@@ -26,6 +26,11 @@
  *    partial results" convention.
  *  - Every spin-wait inside the kernels gives up after about 2 s and raises
  *    a device status word; qi21_device_status() reads and clears it.
+ *  - Entry points may be called from several host threads at once, each on
+ *    its own stream and buffers; the library's one-time set-up is
+ *    thread-safe. A thread with no current CUDA context gets the current
+ *    device's primary context bound on its first call (as the CUDA runtime
+ *    does on a thread's first runtime call).
  */
 #ifndef QI21_H
 #define QI21_H
