@@ -85,14 +85,14 @@ def class_work(w, n_rows, vis_sum):
 # (profiles/dram_traffic_step32_cond4114_n4096.md). Reported only while the
 # source is unchanged.
 NCU_TRAFFIC = {
-    "attention": ("k_attn.cu", "a2ffc7192710e63f6af1716b7e9949804dea9705a429680f5d27ea565cf17e83",
-                  (168189184 + 168228096) // 2 + (21861120 + 19226880) // 2),
-    "gateup": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
-               (252058880 + 253903360) // 2 + (87711232 + 87821312) // 2),
-    "o": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
-          (148278528 + 147124736) // 2 + (31460864 + 31491072) // 2),
-    "down": ("k_gemm.cu", "53a5369e707a6163c422b17cde15463042b7cbceb9c4e391b6af980ca3f541c6",
-             (587750912 + 587684864) // 2 + (59443456 + 59263232) // 2),
+    "attention": ("k_attn.cu", "369265344b3e59f02e4260160ebae98539b6797f1009286c684cbe769b471468",
+                  (168268544 + 168221440) // 2 + (22227968 + 18933504) // 2),
+    "gateup": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
+               (247400960 + 248533504) // 2 + (86342656 + 86459136) // 2),
+    "o": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
+          (149357312 + 147927808) // 2 + (30838528 + 30918144) // 2),
+    "down": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
+             (587621376 + 587564032) // 2 + (59351808 + 59314944) // 2),
 }
 
 
