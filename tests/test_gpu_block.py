@@ -41,7 +41,7 @@ def host(t):
     return t.cpu().numpy()
 
 
-class GpuRun:
+class DeviceRun:
     """Prefill + one step of a workload on the GPU with per-block outputs."""
 
     def __init__(self, w, layers=None, keep_prefill_x=True):
@@ -129,7 +129,7 @@ SMALL = ["tiny_block_d256", "chain32_d256_mixed", "ragged_d512", "cfg_pair_d256"
 @pytest.mark.parametrize("name", SMALL)
 def test_small_workload_end_to_end_and_teacher_forced(name):
     w = S.WORKLOADS[name]
-    run = GpuRun(w)
+    run = DeviceRun(w)
     cfg = O.cfg_of(w)
     weights = [S.layer_weights(w, l) for l in range(w.layers)]
     for s in range(w.nseq):
@@ -213,7 +213,7 @@ def _sample_rows(n, seed):
 
 def test_block_d4096_n4096_sampled():
     w = S.WORKLOADS["block_d4096_n4096"]
-    run = GpuRun(w)
+    run = DeviceRun(w)
     cfg = O.cfg_of(w)
     W = S.layer_weights(w, 0)
     rows = _sample_rows(w.n_target, 1)
@@ -238,7 +238,7 @@ def layers32():
 ])
 def test_full_width_32_layers_sampled(name, layers_checked, layers32):
     w = S.WORKLOADS[name]
-    run = GpuRun(w, layers=layers32)
+    run = DeviceRun(w, layers=layers32)
     cfg = O.cfg_of(w)
     rows = _sample_rows(w.n_target, 2)
     for l in layers_checked:
