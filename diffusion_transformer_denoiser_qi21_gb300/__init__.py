@@ -19,7 +19,7 @@ __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
     "timestep_mods", "denoise", "set_checks", "PackedLayerFp8", "pack_layer_fp8", "workspace_bytes_fp8",
-    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "build",
+    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "selftest_wait_timeout", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -443,3 +443,10 @@ def op_attention(panel, heads, out, nq, n_own, kv_pre=None, n_pre=0, vis=None, s
                                    _ptr(kv_pre, torch.float16, "kv_pre"), n_pre, n_own,
                                    _ptr(vis, torch.int32, "vis"), _ptr(out, torch.float16, "out"),
                                    _stream(stream)))
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the bounded-wait self-test (qi21_selftest_wait_timeout): one
+    CTA whose wait nothing ends gives up after about 2 s and raises the
+    device status word."""
+    check(load().qi21_selftest_wait_timeout(_stream(stream)))

@@ -103,6 +103,7 @@ _SIGS = {
                                _vp]),
     "qi21_step_noalloc": (C.c_int, [C.POINTER(Geom), C.POINTER(Layer), _vp, _vp, _vp, _vp, _vp]),
     "qi21_device_status": (C.c_int, []),
+    "qi21_selftest_wait_timeout": (C.c_int, [_vp]),
     "qi21_profile_enable": (C.c_int, [C.c_int]),
     "qi21_profile_read": (C.c_int, [_vp, _vp]),
     "qi21_op_rowop": (C.c_int, [_i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),

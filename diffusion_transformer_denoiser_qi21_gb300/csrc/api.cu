@@ -63,7 +63,7 @@ int sm_count() {
 
 unsigned int read_and_clear_status() {
   cudaDeviceSynchronize();
-  return gemm_status_read_clear() | attn_status_read_clear();
+  return gemm_status_read_clear() | attn_status_read_clear() | probe_status_read_clear();
 }
 
 // ---------------------------------------------------------- profiling ----
@@ -541,6 +541,11 @@ int qi21_kvcache_layer(const qi21_kvcache* c, int32_t layer, const void** kv) {
 }
 
 int qi21_device_status(void) { return static_cast<int>(read_and_clear_status()); }
+
+int qi21_selftest_wait_timeout(void* stream) {
+  QI21_CK(launch_wait_probe(static_cast<cudaStream_t>(stream)), "wait probe");
+  return QI21_OK;
+}
 
 int qi21_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);

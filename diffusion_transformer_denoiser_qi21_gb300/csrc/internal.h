@@ -133,6 +133,8 @@ bool profiling_on();
 // status word; these read and clear them (after a device synchronise).
 unsigned int gemm_status_read_clear();
 unsigned int attn_status_read_clear();
+unsigned int probe_status_read_clear();
+cudaError_t launch_wait_probe(cudaStream_t s);
 unsigned int read_and_clear_status();
 
 }  // namespace qi21

@@ -320,4 +320,35 @@ cudaError_t count_nonfinite(const void* x, size_t count, int elem_bytes, unsigne
   return cudaSuccess;
 }
 
+// ---------------------------------------------------- bounded-wait test ----
+// One CTA waits on an mbarrier that nothing arrives at, with the same
+// bounded wait every kernel of the library uses: it gives up after the
+// limit, raises the status word and returns, leaving the context usable.
+static __device__ unsigned int s_probe_status = 0;
+
+unsigned int probe_status_read_clear() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, s_probe_status, sizeof v);
+  cudaMemcpyToSymbol(s_probe_status, &z, sizeof z);
+  return v;
+}
+
+__global__ void wait_probe_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // no thread ever arrives: the phase never completes
+  mbar_wait(&bar, 0, &abort_flag, &s_probe_status);
+}
+
+cudaError_t launch_wait_probe(cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
 }  // namespace qi21

@@ -412,6 +412,15 @@ int qi21_graph_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers,
  * gave up waiting). Synchronises the device. */
 int qi21_device_status(void);
 
+/* Self-test of the kernels' bounded waits: enqueues on `stream` one CTA
+ * that waits on an mbarrier nothing arrives at, through the same bounded
+ * wait the library's kernels use. After about 2 s the wait gives up, the
+ * kernel raises the device status word and returns; the context stays
+ * usable, so the next qi21_device_status() returns nonzero and the one
+ * after it 0. Returns QI21_OK once enqueued. For tests of the failure
+ * path; no other entry point is affected. */
+int qi21_selftest_wait_timeout(void* stream);
+
 /* Kernel classes of a pass, for qi21_profile_read. */
 #define QI21_CLASS_ROWOP 0     /* modulated LayerNorm rows */
 #define QI21_CLASS_QKV 1       /* qkv projection (tcgen05 GEMM, f16 panel) */

@@ -100,3 +100,23 @@ def test_checks_pass_on_finite_work_and_refuse_planted_values():
     q.denoise(dw.g, dw.layers, dw.caches[0], tok, w_in, dw.mods_t, fs, w_bad, out, dw.ws)
     torch.cuda.synchronize()
     assert q.count_nonfinite(out) > 0
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    # a wait that nothing ends: the kernel gives up after its limit (~2 s),
+    # raises the status word and returns; no fault, the context stays usable
+    import time
+    assert q.device_status() == 0
+    t0 = time.monotonic()
+    q.selftest_wait_timeout()
+    torch.cuda.synchronize()
+    dt = time.monotonic() - t0
+    assert 1.0 < dt < 30.0, dt
+    assert q.device_status() != 0
+    assert q.device_status() == 0  # read and cleared
+    a = _planted(4096, np.float32, 11)
+    assert q.count_nonfinite(torch.from_numpy(a).cuda()) == int(np.count_nonzero(~np.isfinite(a)))
+    w, dw, _ = _tiny()
+    dw.prefill_all()
+    dw.step()
+    torch.cuda.synchronize()
