@@ -43,7 +43,22 @@ def parse(argv=None):
                    help="query rows of the CPU sample (0 = all target rows)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) variant leg")
+    p.add_argument("--source-shas", action="store_true",
+                   help="print the source hashes the DRAM traffic records are keyed by, and exit")
+    p.add_argument("--dtype", default="f16", choices=["f16", "bf16"],
+                   help="16-bit type of the weights and activation rows (the metric is quoted on f16)")
     return p.parse_args(argv)
+
+
+def workload_of(args):
+    """The named workload in the requested 16-bit type."""
+    import dataclasses
+
+    from synthetic import qi21_inputs as S
+    w = S.WORKLOADS[args.workload]
+    if w.dtype != args.dtype:
+        w = dataclasses.replace(w, name=f"{w.name}_{args.dtype}", dtype=args.dtype)
+    return w
 
 
 # ------------------------------------------------------------ accounting --
@@ -79,35 +94,37 @@ def class_work(w, n_rows, vis_sum):
     }
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
-# of two launches) from one single-pass ncu capture of this benchmark's
-# default workload, with the sha256 of the kernel's source at capture time
-# (profiles/dram_traffic_step32_cond4114_n4096.md). Reported only while the
-# source is unchanged.
-NCU_TRAFFIC = {
-    "attention": ("k_attn.cu", "369265344b3e59f02e4260160ebae98539b6797f1009286c684cbe769b471468",
-                  (168268544 + 168221440) // 2 + (22227968 + 18933504) // 2),
-    "gateup": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
-               (247400960 + 248533504) // 2 + (86342656 + 86459136) // 2),
-    "o": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
-          (149357312 + 147927808) // 2 + (30838528 + 30918144) // 2),
-    "down": ("k_gemm.cu", "ea0d47d7091e576e78ab19204803ded61e42a6cf0809671d0943d50f9d67423b",
-             (587621376 + 587564032) // 2 + (59351808 + 59314944) // 2),
-}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each kernel class, from an ncu capture of a few launches of the one-layer
+# workload block_cond4114_n4096, whose launches have exactly the shapes of a
+# layer of the default workload, with the sha256 of the kernel's sources at
+# capture time. Reported only while those sources are unchanged.
+NCU_TRAFFIC = {}
+
+# The workloads whose launches have the captured shapes.
+TRAFFIC_WORKLOADS = ("step32_cond4114_n4096", "block_cond4114_n4096")
+
+
+def kernel_source_sha(fname):
+    """sha256 over a kernel's translation unit and the headers it includes
+    from csrc/ (ptx.cuh, internal.h)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in (fname, "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "diffusion_transformer_denoiser_qi21_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def measured_traffic(kernel_class, workload):
     """ncu DRAM bytes per launch of a kernel class, or None if there is no
-    capture for this workload or the kernel's source changed since."""
-    import hashlib
-    if workload != DEFAULT_WORKLOAD or kernel_class not in NCU_TRAFFIC:
+    capture for this workload or the kernel's sources changed since."""
+    if workload not in TRAFFIC_WORKLOADS or kernel_class not in NCU_TRAFFIC:
         return None
     fname, sha, nbytes = NCU_TRAFFIC[kernel_class]
-    path = os.path.join(ROOT, "diffusion_transformer_denoiser_qi21_gb300", "csrc", fname)
     try:
-        with open(path, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != sha:
-                return None
+        if kernel_source_sha(fname) != sha:
+            return None
     except OSError:
         return None
     return float(nbytes)
@@ -267,25 +284,33 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    from synthetic import qi21_inputs as S
-    w = S.WORKLOADS[args.workload]
+    w = workload_of(args)
     r = args.cpu_rows if args.cpu_rows > 0 else 128
     smp = OracleSample(w)
     desc = smp.describe(r)
-    times = []
+    times, spent = [], []
     for i in range(args.warmup + args.steps):
-        t_layer, _ = smp.layer_seconds(r)
+        t_layer, t_spent = smp.layer_seconds(r)
         if i >= args.warmup:
             times.append(t_layer)
+            spent.append(t_spent)
     t_layer = statistics.median(times)
     value = w.n_target / (t_layer * w.layers)
     ms = t_layer * w.layers * 1e3
     cores = cpu_cores()
+    n_q = w.n_target if r <= 0 else min(r, w.n_target)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _config(w, args.gpus),
+        # each "step" is a timed sample of one layer, scaled to the whole
+        # step: ms_per_step is that estimate, not a measured step
+        "extrapolated": True,
+        "measured": {"seconds_per_sample": statistics.median(spent), "samples": len(spent),
+                     "what": f"layer 0 of {w.layers}: K/V of all {w.n_target} target rows + the query side "
+                             f"of {n_q} rows"},
+        "extrapolation": {"query_rows_factor": w.n_target / n_q, "layers_factor": w.layers},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -322,7 +347,7 @@ def run_gpu(args):
     from synthetic import qi21_inputs as S
 
     make()
-    w = S.WORKLOADS[args.workload]
+    w = workload_of(args)
     t0 = time.perf_counter()
     dw = D.DeviceWorkload(w)
     torch.cuda.synchronize()
@@ -520,7 +545,7 @@ def run_gpu(args):
     # the FP8 (E4M3 W8A8) variant of the same step, reported beside the
     # f16 headline (its own precision; not the metric's)
     fp8 = None
-    if not args.no_fp8:
+    if not args.no_fp8 and w.dtype == "f16":
         l8 = [q.pack_layer_fp8(dw.g, l) for l in dw.layers]
         ws8 = torch.empty(q.workspace_bytes_fp8(dw.g, max([n_rows] + lp)), dtype=torch.uint8, device="cuda")
         for s_, c_ in enumerate(dw.caches):
@@ -575,7 +600,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": _config(w, world), "tflops": tflops, "flops_per_step": flops_step,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
             "clocks": clk, "classes": classes, "fractions": fractions,
@@ -594,6 +619,9 @@ def run_gpu(args):
 
 def main(argv=None):
     args = parse(argv)
+    if args.source_shas:
+        print(json.dumps({f: kernel_source_sha(f) for f in ("k_gemm.cu", "k_attn.cu", "k_rows.cu")}))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

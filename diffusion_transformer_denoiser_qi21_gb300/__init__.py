@@ -11,7 +11,8 @@ from __future__ import annotations
 import ctypes as C
 
 from . import _binding as B
-from ._binding import (EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE, SEG_TEXT, Geom, Qi21Error,  # noqa: F401
+from ._binding import (DTYPE_BF16, DTYPE_F16, EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU, SEG_IMAGE,  # noqa: F401
+                       SEG_TEXT, Geom, Qi21Error,
                        CLASSES, check, device_status, exported_symbols, profile_enable, profile_read, geom, layer_plane_bytes, layout_indices,
                        layout_rows, load, workspace_bytes)
 
@@ -48,6 +49,22 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def dtype_of(g):
+    """The torch dtype of a geometry's 16-bit buffers."""
+    torch = _torch()
+    return torch.bfloat16 if int(getattr(g, "dtype", 0)) == DTYPE_BF16 else torch.float16
+
+
+def _dt_code(t):
+    """QI21_DTYPE_* of a 16-bit torch tensor."""
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return DTYPE_F16
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"expected an f16 or bf16 tensor, got {t.dtype}")
+
+
 def _stream(stream):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -66,7 +83,8 @@ class PackedLayer:
 
 
 def pack_layer(g: Geom, wq, wk, wv, wo, wgate, wup, wdown, norm_q, norm_k, stream=None) -> PackedLayer:
-    """qi21_pack_layer: f16 device weights in nn.Linear layout -> packed planes."""
+    """qi21_pack_layer: device weights of the geometry's dtype (f16 or bf16)
+    in nn.Linear layout -> packed planes."""
     torch = _torch()
     lib = load()
     nbytes = lib.qi21_layer_plane_bytes(C.byref(g))
@@ -74,7 +92,7 @@ def pack_layer(g: Geom, wq, wk, wv, wo, wgate, wup, wdown, norm_q, norm_k, strea
         check(lib.qi21_geom_check(C.byref(g)))
     planes = torch.empty(nbytes, dtype=torch.uint8, device=wq.device)
     out = B.Layer()
-    h = torch.float16
+    h = dtype_of(g)
     nq = norm_q.contiguous()
     nk = norm_k.contiguous()
     check(lib.qi21_pack_layer(C.byref(g), _ptr(wq, h, "wq"), _ptr(wk, h, "wk"), _ptr(wv, h, "wv"),
@@ -112,8 +130,11 @@ class KVCache:
         return p.value
 
     def layer_tensor(self, layer: int):
-        """A torch f16 [lp, 2H] copy of layer `layer`'s K|V (for checks)."""
-        return _device_view(self.layer_ptr(layer), (self.lp, 2 * self.g.dim), "<f2").clone()
+        """A torch [lp, 2H] copy of layer `layer`'s K|V in the geometry's
+        dtype (for checks)."""
+        torch = _torch()
+        raw = _device_view(self.layer_ptr(layer), (self.lp, 2 * self.g.dim), "<i2").clone()
+        return raw.view(dtype_of(self.g))
 
     def free(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
@@ -262,12 +283,12 @@ def set_checks(flags: int) -> int:
 
 
 def count_nonfinite(x, stream=None) -> int:
-    """qi21_count_nonfinite: NaN/Inf count of a CUDA f32 or f16 tensor
+    """qi21_count_nonfinite: NaN/Inf count of a CUDA f32, f16 or bf16 tensor
     (synchronises the stream)."""
     torch = _torch()
-    eb = {torch.float32: 4, torch.float16: 2}.get(x.dtype)
+    eb = {torch.float32: B.ELEM_F32, torch.float16: B.ELEM_F16, torch.bfloat16: B.ELEM_BF16}.get(x.dtype)
     if eb is None:
-        raise TypeError("count_nonfinite takes f32 or f16 tensors")
+        raise TypeError("count_nonfinite takes f32, f16 or bf16 tensors")
     out = C.c_uint64(0)
     check(load().qi21_count_nonfinite(_ptr(x, x.dtype, "x"), x.numel(), eb, C.byref(out), _stream(stream)))
     return int(out.value)
@@ -399,11 +420,13 @@ def op_gemm_fp8(epi, A, sa, Bw, sw, out, gate_t=None, stream=None):
 # ------------------------------------------------------- single operations --
 
 def op_rowop(x, scale, xn=None, y=None, gate_t=None, eps=1e-6, stream=None):
+    """qi21_op_rowop; xn (f16 or bf16) selects the dtype."""
     torch = _torch()
     rows, dim = x.shape
-    check(load().qi21_op_rowop(rows, dim, eps, _ptr(x, torch.float32, "x"), _ptr(y, torch.float32, "y"),
+    dt = _dt_code(xn) if xn is not None else DTYPE_F16
+    check(load().qi21_op_rowop(dt, rows, dim, eps, _ptr(x, torch.float32, "x"), _ptr(y, torch.float32, "y"),
                                _ptr(gate_t, torch.float32, "gate_t"), _ptr(scale, torch.float32, "scale"),
-                               _ptr(xn, torch.float16, "xn"), _stream(stream)))
+                               _ptr(xn, None, "xn"), _stream(stream)))
 
 
 def op_mods_prep(mods, md, stream=None):
@@ -413,35 +436,37 @@ def op_mods_prep(mods, md, stream=None):
 
 
 def op_gemm(epi, A, Bw, out, gate_t=None, stream=None):
+    """qi21_op_gemm; A and B both f16 or both bf16."""
     torch = _torch()
     M, K = A.shape
     N = Bw.shape[0]
-    check(load().qi21_op_gemm(epi, M, N, K, _ptr(A, torch.float16, "A"), _ptr(Bw, torch.float16, "B"),
+    check(load().qi21_op_gemm(_dt_code(A), epi, M, N, K, _ptr(A, None, "A"), _ptr(Bw, A.dtype, "B"),
                               _ptr(out, None, "out"), out.shape[1], _ptr(gate_t, torch.float32, "gate_t"),
                               _stream(stream)))
 
 
 def op_qkrope(panel, heads, norm_q, norm_k, cos_, sin_, eps=1e-6, stream=None):
     torch = _torch()
-    check(load().qi21_op_qkrope(panel.shape[0], heads, eps, _ptr(panel, torch.float16, "panel"),
+    check(load().qi21_op_qkrope(_dt_code(panel), panel.shape[0], heads, eps, _ptr(panel, None, "panel"),
                                 _ptr(norm_q, torch.float32, "norm_q"), _ptr(norm_k, torch.float32, "norm_k"),
                                 _ptr(cos_, torch.float32, "cos"), _ptr(sin_, torch.float32, "sin"),
                                 _stream(stream)))
 
 
 def op_kvcopy(panel, kv, stream=None):
-    torch = _torch()
     rows = panel.shape[0]
     dim = panel.shape[1] // 3
-    check(load().qi21_op_kvcopy(rows, dim, _ptr(panel, torch.float16, "panel"), _ptr(kv, torch.float16, "kv"),
+    _dt_code(panel)
+    check(load().qi21_op_kvcopy(rows, dim, _ptr(panel, None, "panel"), _ptr(kv, panel.dtype, "kv"),
                                 _stream(stream)))
 
 
 def op_attention(panel, heads, out, nq, n_own, kv_pre=None, n_pre=0, vis=None, stream=None):
+    """qi21_op_attention; panel, kv_pre and out all f16 or all bf16."""
     torch = _torch()
-    check(load().qi21_op_attention(nq, heads, _ptr(panel, torch.float16, "panel"),
-                                   _ptr(kv_pre, torch.float16, "kv_pre"), n_pre, n_own,
-                                   _ptr(vis, torch.int32, "vis"), _ptr(out, torch.float16, "out"),
+    check(load().qi21_op_attention(_dt_code(panel), nq, heads, _ptr(panel, None, "panel"),
+                                   _ptr(kv_pre, panel.dtype, "kv_pre"), n_pre, n_own,
+                                   _ptr(vis, torch.int32, "vis"), _ptr(out, panel.dtype, "out"),
                                    _stream(stream)))
 
 

@@ -25,6 +25,8 @@ ERR = {
 SEG_TEXT = 0
 SEG_IMAGE = 1
 EPI_F16, EPI_F32, EPI_RESID, EPI_SWIGLU = 0, 1, 2, 3
+DTYPE_F16, DTYPE_BF16 = 0, 1
+ELEM_F16, ELEM_BF16, ELEM_F32 = 2, 3, 4
 
 
 class Qi21Error(RuntimeError):
@@ -42,7 +44,7 @@ class LayerFp8(C.Structure):
 class Geom(C.Structure):
     _fields_ = [("dim", C.c_int32), ("heads", C.c_int32), ("head_dim", C.c_int32),
                 ("mlp_hidden", C.c_int32), ("layers", C.c_int32), ("axes", C.c_int32 * 3),
-                ("eps", C.c_float), ("theta", C.c_float)]
+                ("eps", C.c_float), ("theta", C.c_float), ("dtype", C.c_int32)]
 
 
 class Seg(C.Structure):
@@ -106,12 +108,12 @@ _SIGS = {
     "qi21_selftest_wait_timeout": (C.c_int, [_vp]),
     "qi21_profile_enable": (C.c_int, [C.c_int]),
     "qi21_profile_read": (C.c_int, [_vp, _vp]),
-    "qi21_op_rowop": (C.c_int, [_i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "qi21_op_rowop": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_op_mods_prep": (C.c_int, [_i32, _vp, _vp, _vp]),
-    "qi21_op_gemm": (C.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
-    "qi21_op_qkrope": (C.c_int, [_i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "qi21_op_gemm": (C.c_int, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "qi21_op_qkrope": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_op_kvcopy": (C.c_int, [_i32, _i32, _vp, _vp, _vp]),
-    "qi21_op_attention": (C.c_int, [_i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "qi21_op_attention": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -143,11 +145,16 @@ def check(rc: int) -> None:
         raise Qi21Error(rc, load().qi21_last_error().decode())
 
 
-def geom(dim, heads, mlp_hidden, layers, axes=(16, 56, 56), eps=1e-6, theta=10000.0, head_dim=128) -> Geom:
+def geom(dim, heads, mlp_hidden, layers, axes=(16, 56, 56), eps=1e-6, theta=10000.0, head_dim=128,
+         dtype=DTYPE_F16) -> Geom:
+    """qi21_geom; dtype DTYPE_F16 / DTYPE_BF16 (or "f16" / "bf16")."""
+    if isinstance(dtype, str):
+        dtype = {"f16": DTYPE_F16, "bf16": DTYPE_BF16}[dtype]
     g = Geom()
     g.dim, g.heads, g.head_dim, g.mlp_hidden, g.layers = dim, heads, head_dim, mlp_hidden, layers
     g.axes[:] = list(axes)
     g.eps, g.theta = eps, theta
+    g.dtype = dtype
     return g
 
 

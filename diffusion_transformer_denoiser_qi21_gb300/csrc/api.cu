@@ -14,6 +14,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/qi21.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -51,14 +53,15 @@ bool bind_primary_context() {
 }
 
 int sm_count() {
-  // initialised once, thread-safely, on first use
-  static const int n = [] {
+  // initialised once per device, thread-safely, on first use there
+  static PerDevice<int> once;
+  const int* n = once.get([] {
     int dev = 0, v = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
     return v > 0 ? v : 1;
-  }();
-  return n;
+  });
+  return n ? *n : 1;
 }
 
 unsigned int read_and_clear_status() {
@@ -237,8 +240,21 @@ static int geom_check(const qi21_geom* g) {
   if (g->axes[0] + g->axes[1] + g->axes[2] != g->head_dim)
     return fail(QI21_ERR_GEOM, "RoPE axes do not tile head_dim");
   if (!(g->eps > 0.f) || !(g->theta > 0.f)) return fail(QI21_ERR_GEOM, "eps and theta must be > 0");
+  if (g->dtype != QI21_DTYPE_F16 && g->dtype != QI21_DTYPE_BF16)
+    return fail(QI21_ERR_GEOM, "dtype %d (QI21_DTYPE_F16 or QI21_DTYPE_BF16)", g->dtype);
   return QI21_OK;
 }
+
+// The FP8 variant quantises f16 planes and f16 activation rows.
+static int geom_check_fp8(const qi21_geom* g) {
+  const int rc = geom_check(g);
+  if (rc != QI21_OK) return rc;
+  if (g->dtype != QI21_DTYPE_F16) return fail(QI21_ERR_GEOM, "the FP8 variant takes f16 geometries only");
+  return QI21_OK;
+}
+
+// Element type of the geometry's 16-bit buffers for the finite scan.
+static int elem_of(const qi21_geom* g) { return g->dtype == QI21_DTYPE_BF16 ? QI21_ELEM_BF16 : QI21_ELEM_F16; }
 
 // -------------------------------------------------------------- sizes ----
 
@@ -288,7 +304,7 @@ struct qi21_kvcache {
   std::vector<qi21_seg> segs;
   int lp = 0, n = 0;
   void* mem = nullptr;  // one allocation: kv, vis, tables
-  __half* kv = nullptr;  // [L][lp][2H]
+  void* kv = nullptr;  // [L][lp][2H] of the geometry's dtype
   uint32_t* vis = nullptr;
   float* cos_p = nullptr;
   float* sin_p = nullptr;
@@ -358,12 +374,12 @@ size_t qi21_workspace_bytes(const qi21_geom* g, int32_t max_rows) {
 }
 
 size_t qi21_workspace_bytes_fp8(const qi21_geom* g, int32_t max_rows) {
-  if (geom_check(g) != QI21_OK || max_rows < 0) return 0;
+  if (geom_check_fp8(g) != QI21_OK || max_rows < 0) return 0;
   return ws_layout(g, max_rows, true).total;
 }
 
 size_t qi21_layer_fp8_bytes(const qi21_geom* g) {
-  if (geom_check(g) != QI21_OK) return 0;
+  if (geom_check_fp8(g) != QI21_OK) return 0;
   const size_t H = g->dim, I = g->mlp_hidden;
   return align256(3 * H * H) + align256(H * H) + align256(2 * I * H) + align256(H * I) + align256(3 * H * 4) +
          align256(H * 4) + align256(2 * I * 4) + align256(H * 4);
@@ -385,10 +401,10 @@ int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const vo
   const size_t H = g->dim, I = g->mlp_hidden;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(planes);
-  __half* wqkv = reinterpret_cast<__half*>(base);
-  __half* pwo = reinterpret_cast<__half*>(base + align256(3 * H * H * 2));
-  __half* w13 = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(pwo) + align256(H * H * 2));
-  __half* w2 = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(w13) + align256(2 * I * H * 2));
+  uint16_t* wqkv = reinterpret_cast<uint16_t*>(base);
+  uint16_t* pwo = reinterpret_cast<uint16_t*>(base + align256(3 * H * H * 2));
+  uint16_t* w13 = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pwo) + align256(H * H * 2));
+  uint16_t* w2 = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(w13) + align256(2 * I * H * 2));
   cudaError_t e;
   if ((e = cudaMemcpyAsync(wqkv, wq, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
       (e = cudaMemcpyAsync(wqkv + H * H, wk, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
@@ -396,8 +412,7 @@ int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const vo
       (e = cudaMemcpyAsync(pwo, wo, H * H * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
       (e = cudaMemcpyAsync(w2, wdown, H * I * 2, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
     return cuda_fail(e, "pack copies");
-  e = launch_pack_w13(static_cast<int>(I), static_cast<int>(H), static_cast<const __half*>(wgate),
-                      static_cast<const __half*>(wup), w13, s);
+  e = launch_pack_w13(static_cast<int>(I), static_cast<int>(H), wgate, wup, w13, s);
   if (e != cudaSuccess) return cuda_fail(e, "pack_w13");
   out->wqkv = wqkv;
   out->wo = pwo;
@@ -410,7 +425,7 @@ int qi21_pack_layer(const qi21_geom* g, const void* wq, const void* wk, const vo
 
 int qi21_pack_layer_fp8(const qi21_geom* g, const qi21_layer* planes, void* mem, size_t bytes, qi21_layer_fp8* out,
                         void* stream) {
-  int rc = geom_check(g);
+  int rc = geom_check_fp8(g);
   if (rc != QI21_OK) return rc;
   if (!planes || !mem || !out) return fail(QI21_ERR_ARG, "null pointer");
   if (!planes->wqkv || !planes->wo || !planes->w13 || !planes->w2 || !planes->norm_q || !planes->norm_k)
@@ -496,7 +511,7 @@ int qi21_kvcache_alloc(const qi21_geom* g, const qi21_seg* segs, int32_t nseg, q
     return cuda_fail(e, "kv cache allocation");
   }
   uint8_t* b = static_cast<uint8_t*>(cc->mem);
-  cc->kv = reinterpret_cast<__half*>(b);
+  cc->kv = b;
   cc->vis = reinterpret_cast<uint32_t*>(b + kv_bytes);
   cc->cos_p = reinterpret_cast<float*>(b + kv_bytes + vis_bytes);
   cc->sin_p = reinterpret_cast<float*>(b + kv_bytes + vis_bytes + tp_bytes);
@@ -536,7 +551,7 @@ int qi21_kvcache_info(const qi21_kvcache* c, int32_t* lp, int32_t* n, int32_t* l
 int qi21_kvcache_layer(const qi21_kvcache* c, int32_t layer, const void** kv) {
   if (c == nullptr || kv == nullptr) return fail(QI21_ERR_ARG, "null pointer");
   if (layer < 0 || layer >= c->g.layers) return fail(QI21_ERR_STATE, "layer %d out of range", layer);
-  *kv = c->kv + static_cast<size_t>(layer) * c->lp * 2 * c->g.dim;
+  *kv = static_cast<const uint16_t*>(c->kv) + static_cast<size_t>(layer) * c->lp * 2 * c->g.dim;
   return QI21_OK;
 }
 
@@ -581,7 +596,8 @@ namespace {
 bool same_geom(const qi21_geom& a, const qi21_geom& b) {
   return a.dim == b.dim && a.heads == b.heads && a.head_dim == b.head_dim &&
          a.mlp_hidden == b.mlp_hidden && a.layers == b.layers && a.axes[0] == b.axes[0] &&
-         a.axes[1] == b.axes[1] && a.axes[2] == b.axes[2] && a.eps == b.eps && a.theta == b.theta;
+         a.axes[1] == b.axes[1] && a.axes[2] == b.axes[2] && a.eps == b.eps && a.theta == b.theta &&
+         a.dtype == b.dtype;
 }
 
 int check_layers(const qi21_geom* g, const qi21_layer* layers) {
@@ -613,32 +629,37 @@ int check_layers_fp8(const qi21_geom* g, const qi21_layer_fp8* layers) {
 }
 
 
-// One layer's second half: attention -> O (+gate) -> LN2 -> gate/up -> down
-// (+gate); the first half (LN1, qkv, qkrope) is done by the caller.
+// Buffers of a pass (workspace views; x may be the caller's x_out).
 struct PassBufs {
   float* x;
-  __half* xn;
-  __half* panel;
-  __half* att;
-  __half* hid;
+  void* xn;     // dt [M][H]
+  void* panel;  // dt [M][3H]
+  void* att;    // dt [M][H]
+  void* hid;    // dt [M][I]
   float* md;
   uint8_t* q8;  // FP8 pass: E4M3 activation rows (xn, att, hid in turn)
   float* qs;    // FP8 pass: their row scales
 };
 
-// One pass over the layers. Exactly one of layers (f16 planes) and l8 (the
-// FP8 variant: E4M3 planes, every projection on row-quantised activations)
-// is non-null.
-int run_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8* l8, int M, bool prefill,
-             qi21_kvcache* pcache, const qi21_kvcache* const* caches, int nseq, int n,
-             const PassBufs& b, float* x_layers, cudaStream_t s) {
-  const bool f8 = l8 != nullptr;
-  const int H = g->dim, I = g->mlp_hidden, L = g->layers;
-  const float* s1 = b.md;
-  const float* g1 = b.md + H;
-  const float* s2 = b.md + 2 * H;
-  const float* g2 = b.md + 3 * H;
+// Everything one layer launches, with its tensor maps already encoded.
+struct LayerPlan {
+  GemmPlan pq, po, p13, p2;
+  AttnPlan at;
+  void* kv;       // prefill: the layer's cache block (the K|V copy target)
+  bool has_attn;  // false for the prefill's last layer (stops after its cache write)
+};
 
+// Plans of every layer of a pass, encoded before the pass enqueues anything
+// (so an encoding failure at any layer leaves the stream untouched). Exactly
+// one of layers (16-bit planes) and l8 (the FP8 variant: E4M3 planes, every
+// projection on row-quantised activations) is non-null.
+int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8* l8, int M, bool prefill,
+              qi21_kvcache* pcache, const qi21_kvcache* const* caches, int nseq, int n, const PassBufs& b,
+              std::vector<LayerPlan>& plans) {
+  const bool f8 = l8 != nullptr;
+  const int H = g->dim, I = g->mlp_hidden, L = g->layers, dt = g->dtype;
+  const float* g1 = b.md + H;
+  const float* g2 = b.md + 3 * H;
   RopeTables tabs{};
   if (prefill) {
     tabs.nsrc = 1;
@@ -647,103 +668,126 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8*
     tabs.nsrc = nseq;
     for (int q = 0; q < nseq; ++q) tabs.src[q] = RopeSrc{caches[q]->cos_t, caches[q]->sin_t, q * n};
   }
-
-  // the modulated LayerNorm of x (f16 xn, or E4M3 rows + scales)
-  auto ln = [&](const float* scale) -> int {
-    ProfScope ps(QI21_CLASS_ROWOP, s);
-    if (f8)
-      QI21_CK(launch_rowop_q8(M, H, g->eps, b.x, scale, b.q8, b.qs, s), "rowop q8");
-    else
-      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, scale, b.xn, s), "rowop");
-    return QI21_OK;
-  };
-  // f16 rows -> E4M3 rows + scales (FP8 pass: att and hid)
-  auto quant = [&](const __half* a, int cols) -> int {
-    ProfScope ps(QI21_CLASS_QUANT, s);
-    QI21_CK(launch_quant_rows(M, cols, a, static_cast<size_t>(cols), b.q8, static_cast<size_t>(cols), b.qs, s),
-            "quantise rows");
-    return QI21_OK;
-  };
-  int rc;
-  if ((rc = ln(s1)) != QI21_OK) return rc;
+  plans.resize(L);
   for (int l = 0; l < L; ++l) {
+    LayerPlan& lp = plans[l];
     const bool last = (l + 1 == L);
     const float* norm_q = f8 ? l8[l].norm_q : layers[l].norm_q;
     const float* norm_k = f8 ? l8[l].norm_k : layers[l].norm_k;
-    GemmPlan pq, po, p13, p2;
     // qkv projection with the qk RMSNorm + RoPE fused into its epilogue
     if (f8)
-      QI21_CK(make_gemm_plan_f8(&pq, EPI_QKV, M, 3 * H, H, b.q8, b.qs, l8[l].wqkv, l8[l].s_qkv, b.panel, 3 * H,
+      QI21_CK(make_gemm_plan_f8(&lp.pq, EPI_QKV, M, 3 * H, H, b.q8, b.qs, l8[l].wqkv, l8[l].s_qkv, b.panel, 3 * H,
                                 nullptr),
               "qkv plan");
     else
-      QI21_CK(make_gemm_plan(&pq, EPI_QKV, M, 3 * H, H, b.xn, static_cast<const __half*>(layers[l].wqkv), b.panel,
-                             3 * H, nullptr),
+      QI21_CK(make_gemm_plan(&lp.pq, EPI_QKV, dt, M, 3 * H, H, b.xn, layers[l].wqkv, b.panel, 3 * H, nullptr),
               "qkv plan");
-    pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs};
-    {
-      ProfScope ps(QI21_CLASS_QKV, s);
-      QI21_CK(launch_gemm(pq, s), "qkv gemm");
-    }
+    lp.pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs};
+    lp.kv = prefill ? static_cast<uint16_t*>(pcache->kv) + static_cast<size_t>(l) * pcache->lp * 2 * H : nullptr;
+    lp.has_attn = !(prefill && last);
+    if (!lp.has_attn) break;
     AttnArgs aa{};
     aa.panel = b.panel;
     aa.panel_rows = M;
     aa.out = b.att;
     aa.heads = g->heads;
+    aa.dt = dt;
     if (prefill) {
-      __half* kv = pcache->kv + static_cast<size_t>(l) * pcache->lp * 2 * H;
-      {
-        ProfScope ps(QI21_CLASS_KVCOPY, s);
-        QI21_CK(launch_kvcopy(M, H, b.panel, kv, s), "kvcopy");
-      }
-      if (last) break;
       aa.nseq = 1;
       aa.seq[0] = AttnSeq{nullptr, 0, 0, M, 0, M, pcache->vis};
     } else {
       aa.nseq = nseq;
       for (int q = 0; q < nseq; ++q) {
         const qi21_kvcache* c = caches[q];
-        aa.seq[q] = AttnSeq{c->kv + static_cast<size_t>(l) * c->lp * 2 * H, c->lp, q * n, n, q * n, n,
-                            nullptr};
+        aa.seq[q] = AttnSeq{static_cast<const uint16_t*>(c->kv) + static_cast<size_t>(l) * c->lp * 2 * H, c->lp,
+                            q * n, n, q * n, n, nullptr};
       }
     }
+    QI21_CK(make_attn_plan(aa, &lp.at), "attention plan");
+    if (f8) {
+      QI21_CK(make_gemm_plan_f8(&lp.po, EPI_RESID, M, H, H, b.q8, b.qs, l8[l].wo, l8[l].s_o, b.x, H, g1), "o plan");
+      QI21_CK(make_gemm_plan_f8(&lp.p13, EPI_SWIGLU, M, 2 * I, H, b.q8, b.qs, l8[l].w13, l8[l].s_13, b.hid, I,
+                                nullptr),
+              "w13 plan");
+      QI21_CK(make_gemm_plan_f8(&lp.p2, EPI_RESID, M, H, I, b.q8, b.qs, l8[l].w2, l8[l].s_2, b.x, H, g2),
+              "down plan");
+    } else {
+      QI21_CK(make_gemm_plan(&lp.po, EPI_RESID, dt, M, H, H, b.att, layers[l].wo, b.x, H, g1), "o plan");
+      QI21_CK(make_gemm_plan(&lp.p13, EPI_SWIGLU, dt, M, 2 * I, H, b.xn, layers[l].w13, b.hid, I, nullptr),
+              "w13 plan");
+      QI21_CK(make_gemm_plan(&lp.p2, EPI_RESID, dt, M, H, I, b.hid, layers[l].w2, b.x, H, g2), "down plan");
+    }
+  }
+  return QI21_OK;
+}
+
+// NVTX range around the launches of one layer.
+class LayerRange {
+ public:
+  LayerRange(bool prefill, int l) {
+    char name[48];
+    snprintf(name, sizeof name, "qi21 %s layer %d", prefill ? "prefill" : "step", l);
+    nvtxRangePushA(name);
+  }
+  ~LayerRange() { nvtxRangePop(); }
+};
+
+// The launches of a planned pass, in order, on stream s.
+int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& b,
+              const std::vector<LayerPlan>& plans, float* x_layers, cudaStream_t s) {
+  const int H = g->dim, I = g->mlp_hidden, L = g->layers, dt = g->dtype;
+  const float* s1 = b.md;
+  const float* s2 = b.md + 2 * H;
+  // the modulated LayerNorm of x (16-bit xn, or E4M3 rows + scales)
+  auto ln = [&](const float* scale) -> int {
+    ProfScope ps(QI21_CLASS_ROWOP, s);
+    if (f8)
+      QI21_CK(launch_rowop_q8(M, H, g->eps, b.x, scale, b.q8, b.qs, s), "rowop q8");
+    else
+      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, scale, b.xn, dt, s), "rowop");
+    return QI21_OK;
+  };
+  // f16 rows -> E4M3 rows + scales (FP8 pass: att and hid)
+  auto quant = [&](const void* a, int cols) -> int {
+    ProfScope ps(QI21_CLASS_QUANT, s);
+    QI21_CK(launch_quant_rows(M, cols, static_cast<const __half*>(a), static_cast<size_t>(cols), b.q8,
+                              static_cast<size_t>(cols), b.qs, s),
+            "quantise rows");
+    return QI21_OK;
+  };
+  int rc;
+  if ((rc = ln(s1)) != QI21_OK) return rc;
+  for (int l = 0; l < L; ++l) {
+    const LayerRange range(prefill, l);
+    const LayerPlan& lp = plans[l];
+    const bool last = (l + 1 == L);
+    {
+      ProfScope ps(QI21_CLASS_QKV, s);
+      QI21_CK(launch_gemm(lp.pq, s), "qkv gemm");
+    }
+    if (prefill) {
+      ProfScope ps(QI21_CLASS_KVCOPY, s);
+      QI21_CK(launch_kvcopy(M, H, b.panel, lp.kv, s), "kvcopy");
+    }
+    if (!lp.has_attn) break;
     {
       ProfScope ps(QI21_CLASS_ATTENTION, s);
-      QI21_CK(launch_attention(aa, s), "attention");
+      QI21_CK(launch_attn_plan(lp.at, s), "attention");
     }
-    if (f8) {
-      if ((rc = quant(b.att, H)) != QI21_OK) return rc;
-      QI21_CK(make_gemm_plan_f8(&po, EPI_RESID, M, H, H, b.q8, b.qs, l8[l].wo, l8[l].s_o, b.x, H, g1), "o plan");
-    } else {
-      QI21_CK(make_gemm_plan(&po, EPI_RESID, M, H, H, b.att, static_cast<const __half*>(layers[l].wo), b.x, H, g1),
-              "o plan");
-    }
+    if (f8 && (rc = quant(b.att, H)) != QI21_OK) return rc;
     {
       ProfScope ps(QI21_CLASS_O, s);
-      QI21_CK(launch_gemm(po, s), "o gemm");
+      QI21_CK(launch_gemm(lp.po, s), "o gemm");
     }
     if ((rc = ln(s2)) != QI21_OK) return rc;
-    if (f8)
-      QI21_CK(make_gemm_plan_f8(&p13, EPI_SWIGLU, M, 2 * I, H, b.q8, b.qs, l8[l].w13, l8[l].s_13, b.hid, I, nullptr),
-              "w13 plan");
-    else
-      QI21_CK(make_gemm_plan(&p13, EPI_SWIGLU, M, 2 * I, H, b.xn, static_cast<const __half*>(layers[l].w13), b.hid, I,
-                             nullptr),
-              "w13 plan");
     {
       ProfScope ps(QI21_CLASS_GATEUP, s);
-      QI21_CK(launch_gemm(p13, s), "gate/up gemm");
+      QI21_CK(launch_gemm(lp.p13, s), "gate/up gemm");
     }
-    if (f8) {
-      if ((rc = quant(b.hid, I)) != QI21_OK) return rc;
-      QI21_CK(make_gemm_plan_f8(&p2, EPI_RESID, M, H, I, b.q8, b.qs, l8[l].w2, l8[l].s_2, b.x, H, g2), "down plan");
-    } else {
-      QI21_CK(make_gemm_plan(&p2, EPI_RESID, M, H, I, b.hid, static_cast<const __half*>(layers[l].w2), b.x, H, g2),
-              "down plan");
-    }
+    if (f8 && (rc = quant(b.hid, I)) != QI21_OK) return rc;
     {
       ProfScope ps(QI21_CLASS_DOWN, s);
-      QI21_CK(launch_gemm(p2, s), "down gemm");
+      QI21_CK(launch_gemm(lp.p2, s), "down gemm");
     }
     if (x_layers)
       QI21_CK(cudaMemcpyAsync(x_layers + static_cast<size_t>(l) * M * H, b.x,
@@ -754,6 +798,10 @@ int run_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8*
   return QI21_OK;
 }
 
+// Per-thread plan storage, reused across calls (no allocation per step once
+// it has grown to the largest layer count seen).
+thread_local std::vector<LayerPlan> t_plans;
+
 int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, bool fp8 = false) {
   if (ws == nullptr) return fail(QI21_ERR_WORKSPACE, "null workspace");
   if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(QI21_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -761,10 +809,10 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, b
   if (ws_bytes < w.total) return fail(QI21_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, w.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
   b->x = reinterpret_cast<float*>(base + w.x);
-  b->xn = reinterpret_cast<__half*>(base + w.xn);
-  b->panel = reinterpret_cast<__half*>(base + w.panel);
-  b->att = reinterpret_cast<__half*>(base + w.att);
-  b->hid = reinterpret_cast<__half*>(base + w.hid);
+  b->xn = base + w.xn;
+  b->panel = base + w.panel;
+  b->att = base + w.att;
+  b->hid = base + w.hid;
   b->md = reinterpret_cast<float*>(base + w.md);
   b->q8 = fp8 ? base + w.q8 : nullptr;
   b->qs = fp8 ? reinterpret_cast<float*>(base + w.qs) : nullptr;
@@ -790,11 +838,30 @@ int finite_check(const void* x, size_t count, int eb, const char* what, cudaStre
   return QI21_OK;
 }
 
+// A validated and planned step (the plans are in t_plans).
+struct StepCall {
+  PassBufs b;
+  int M = 0, n = 0;
+};
+
+// Validation and planning of qi21_step_batch (nothing enqueued).
+int step_prepare(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
+                 const float* x_in, float* x_out, const float* mods, void* workspace, size_t ws_bytes,
+                 const qi21_layer_fp8* l8, StepCall* sc);
+// The launches of a prepared step.
+int step_enqueue(const qi21_geom* g, bool f8, const StepCall& sc, const float* x_in, float* x_out,
+                 const float* mods, float* x_layers, cudaStream_t s);
+
 // qi21_step_batch without the finite check (qi21_denoise_batch checks the
 // velocity instead).
 int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
                     const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
-                    size_t ws_bytes, void* stream, const qi21_layer_fp8* l8 = nullptr);
+                    size_t ws_bytes, void* stream, const qi21_layer_fp8* l8 = nullptr) {
+  StepCall sc;
+  const int rc = step_prepare(g, layers, caches, nseq, x_in, x_out, mods, workspace, ws_bytes, l8, &sc);
+  if (rc != QI21_OK) return rc;
+  return step_enqueue(g, l8 != nullptr, sc, x_in, x_out, mods, x_layers, static_cast<cudaStream_t>(stream));
+}
 
 int prefill_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8* l8, qi21_kvcache* cache,
                  const float* x_prefix, const float* mods0, float* x_layers, void* workspace, size_t ws_bytes,
@@ -807,6 +874,9 @@ int prefill_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_
   const int M = cache->lp;
   PassBufs b;
   if ((rc = ws_bind(g, M, workspace, ws_bytes, &b, l8 != nullptr)) != QI21_OK) return rc;
+  // every layer's maps, before anything is enqueued
+  if ((rc = plan_pass(g, l8 ? nullptr : layers, l8, M, true, cache, nullptr, 1, 0, b, t_plans)) != QI21_OK)
+    return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t H = g->dim;
   QI21_CK(cudaMemcpyAsync(b.x, x_prefix, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
@@ -815,10 +885,10 @@ int prefill_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_
     ProfScope ps(QI21_CLASS_MISC, s);
     QI21_CK(launch_mods_prep(g->dim, mods0, b.md, s), "mods prep");
   }
-  rc = run_pass(g, l8 ? nullptr : layers, l8, M, true, cache, nullptr, 1, 0, b, x_layers, s);
+  rc = exec_pass(g, l8 != nullptr, M, true, b, t_plans, x_layers, s);
   if (rc != QI21_OK) return rc;
   cache->filled = true;
-  return finite_check(cache->kv, static_cast<size_t>(g->layers) * M * 2 * H, 2, "the K/V cache", s);
+  return finite_check(cache->kv, static_cast<size_t>(g->layers) * M * 2 * H, elem_of(g), "the K/V cache", s);
 }
 
 }  // namespace
@@ -827,12 +897,14 @@ extern "C" {
 
 uint32_t qi21_set_checks(uint32_t flags) { return g_checks.exchange(flags); }
 
-int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64_t* out_count, void* stream) {
-  if (elem_bytes != 2 && elem_bytes != 4) return fail(QI21_ERR_ARG, "elem_bytes %d (2 or 4)", elem_bytes);
+int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_type, uint64_t* out_count, void* stream) {
+  if (elem_type != QI21_ELEM_F16 && elem_type != QI21_ELEM_BF16 && elem_type != QI21_ELEM_F32)
+    return fail(QI21_ERR_ARG, "elem_type %d (QI21_ELEM_F16, _BF16 or _F32)", elem_type);
   if (out_count == nullptr || (count > 0 && x == nullptr)) return fail(QI21_ERR_ARG, "null pointer");
+  const int elem_bytes = elem_type == QI21_ELEM_F32 ? 4 : 2;
   if (reinterpret_cast<uintptr_t>(x) % elem_bytes) return fail(QI21_ERR_ARG, "x not aligned to its element");
   unsigned long long bad = 0;
-  const int rc = count_bad(x, count, elem_bytes, &bad, static_cast<cudaStream_t>(stream));
+  const int rc = count_bad(x, count, elem_type, &bad, static_cast<cudaStream_t>(stream));
   if (rc != QI21_OK) return rc;
   *out_count = bad;
   return QI21_OK;
@@ -846,18 +918,22 @@ int qi21_prefill(const qi21_geom* g, const qi21_layer* layers, qi21_kvcache* cac
 
 int qi21_prefill_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, qi21_kvcache* cache, const float* x_prefix,
                      const float* mods0, float* x_layers, void* workspace, size_t ws_bytes, void* stream) {
-  if (layers == nullptr && geom_check(g) == QI21_OK) return fail(QI21_ERR_ARG, "null layers");
+  const int gc = geom_check_fp8(g);
+  if (gc != QI21_OK) return gc;
+  if (layers == nullptr) return fail(QI21_ERR_ARG, "null layers");
   return prefill_impl(g, nullptr, layers, cache, x_prefix, mods0, x_layers, workspace, ws_bytes, stream);
 }
 
 int qi21_step_batch_fp8(const qi21_geom* g, const qi21_layer_fp8* layers, const qi21_kvcache* const* caches,
                         int32_t nseq, const float* x_in, float* x_out, const float* mods, float* x_layers,
                         void* workspace, size_t ws_bytes, void* stream) {
-  if (layers == nullptr && geom_check(g) == QI21_OK) return fail(QI21_ERR_ARG, "null layers");
+  const int gc = geom_check_fp8(g);
+  if (gc != QI21_OK) return gc;
+  if (layers == nullptr) return fail(QI21_ERR_ARG, "null layers");
   const int rc =
       step_batch_impl(g, nullptr, caches, nseq, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream, layers);
   if (rc != QI21_OK) return rc;
-  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, 4, "the hidden state",
+  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, QI21_ELEM_F32, "the hidden state",
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -866,7 +942,7 @@ int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
                     void* workspace, size_t ws_bytes, void* stream) {
   const int rc = step_batch_impl(g, layers, caches, nseq, x_in, x_out, mods, x_layers, workspace, ws_bytes, stream);
   if (rc != QI21_OK) return rc;
-  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, 4, "the hidden state",
+  return finite_check(x_out, static_cast<size_t>(nseq) * caches[0]->n * g->dim, QI21_ELEM_F32, "the hidden state",
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -874,9 +950,9 @@ int qi21_step_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
 
 namespace {
 
-int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
-                    const float* x_in, float* x_out, const float* mods, float* x_layers, void* workspace,
-                    size_t ws_bytes, void* stream, const qi21_layer_fp8* l8) {
+int step_prepare(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcache* const* caches, int32_t nseq,
+                 const float* x_in, float* x_out, const float* mods, void* workspace, size_t ws_bytes,
+                 const qi21_layer_fp8* l8, StepCall* sc) {
   int rc = geom_check(g);
   if (rc != QI21_OK) return rc;
   if (caches == nullptr || x_in == nullptr || x_out == nullptr || mods == nullptr)
@@ -892,20 +968,25 @@ int step_batch_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_kvc
     if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
   }
   if ((rc = l8 ? check_layers_fp8(g, l8) : check_layers(g, layers)) != QI21_OK) return rc;
-  const int M = nseq * n;
-  PassBufs b;
-  if ((rc = ws_bind(g, M, workspace, ws_bytes, &b, l8 != nullptr)) != QI21_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  sc->n = n;
+  sc->M = nseq * n;
+  if ((rc = ws_bind(g, sc->M, workspace, ws_bytes, &sc->b, l8 != nullptr)) != QI21_OK) return rc;
+  sc->b.x = x_out;
+  // every layer's maps, before anything is enqueued
+  return plan_pass(g, l8 ? nullptr : layers, l8, sc->M, false, nullptr, caches, nseq, n, sc->b, t_plans);
+}
+
+int step_enqueue(const qi21_geom* g, bool f8, const StepCall& sc, const float* x_in, float* x_out,
+                 const float* mods, float* x_layers, cudaStream_t s) {
   const size_t H = g->dim;
   if (x_out != x_in)
-    QI21_CK(cudaMemcpyAsync(x_out, x_in, static_cast<size_t>(M) * H * 4, cudaMemcpyDeviceToDevice, s),
+    QI21_CK(cudaMemcpyAsync(x_out, x_in, static_cast<size_t>(sc.M) * H * 4, cudaMemcpyDeviceToDevice, s),
             "x copy");
-  b.x = x_out;
   {
     ProfScope ps(QI21_CLASS_MISC, s);
-    QI21_CK(launch_mods_prep(g->dim, mods, b.md, s), "mods prep");
+    QI21_CK(launch_mods_prep(g->dim, mods, sc.b.md, s), "mods prep");
   }
-  return run_pass(g, layers, l8, M, false, nullptr, caches, nseq, n, b, x_layers, s);
+  return exec_pass(g, f8, sc.M, false, sc.b, t_plans, x_layers, s);
 }
 
 }  // namespace
@@ -965,27 +1046,25 @@ int qi21_denoise_batch(const qi21_geom* g, const qi21_layer* layers, const qi21_
   if (rc != QI21_OK) return rc;
   if (caches == nullptr || nseq < 1 || nseq > kMaxSeq) return fail(QI21_ERR_ARG, "caches / nseq");
   if (!tok || !w_in || !mods || !final_scale || !w_out || !out) return fail(QI21_ERR_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(w_in) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(QI21_ERR_ARG, "w_in and out must be 16-byte aligned");
   for (int q = 0; q < nseq; ++q)
     if (caches[q] == nullptr) return fail(QI21_ERR_ARG, "null cache %d", q);
   const int n = caches[0]->n;
   const int M = nseq * n;
   PassBufs b;
   if ((rc = ws_bind(g, M, workspace, ws_bytes, &b)) != QI21_OK) return rc;
-  // the full validation of the step runs before anything is enqueued
-  if ((rc = check_layers(g, layers)) != QI21_OK) return rc;
-  for (int q = 0; q < nseq; ++q) {
-    const qi21_kvcache* c = caches[q];
-    if (!same_geom(*g, c->g)) return fail(QI21_ERR_SHAPE, "cache %d was made for another geometry", q);
-    if (!c->filled) return fail(QI21_ERR_STATE, "cache %d has not been prefilled", q);
-    if (c->n != n) return fail(QI21_ERR_SHAPE, "caches disagree on the target rows (%d vs %d)", c->n, n);
-  }
+  // the whole step is validated and planned before anything is enqueued;
+  // the embedding and the final layer take arguments checked above
+  StepCall sc;
+  if ((rc = step_prepare(g, layers, caches, nseq, b.x, b.x, mods, workspace, ws_bytes, nullptr, &sc)) != QI21_OK)
+    return rc;
   if ((rc = qi21_embed(M, g->dim, QI21_LATENT_CHANNELS, tok, w_in, b.x, stream)) != QI21_OK) return rc;
-  if ((rc = step_batch_impl(g, layers, caches, nseq, b.x, b.x, mods, nullptr, workspace, ws_bytes, stream)) !=
-      QI21_OK)
+  if ((rc = step_enqueue(g, false, sc, b.x, b.x, mods, nullptr, static_cast<cudaStream_t>(stream))) != QI21_OK)
     return rc;
   if ((rc = qi21_final(M, g->dim, QI21_LATENT_CHANNELS, g->eps, b.x, final_scale, w_out, out, stream)) != QI21_OK)
     return rc;
-  return finite_check(out, static_cast<size_t>(M) * QI21_LATENT_CHANNELS, 4, "the velocity",
+  return finite_check(out, static_cast<size_t>(M) * QI21_LATENT_CHANNELS, QI21_ELEM_F32, "the velocity",
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -1109,14 +1188,18 @@ void qi21_graph_free(qi21_graph* gr) {
 
 // ------------------------------------------------------ single operations --
 
-int qi21_op_rowop(int32_t rows, int32_t dim, float eps, float* x, const float* y, const float* gate_t,
+static int dtype_check(int32_t dtype) {
+  if (dtype != QI21_DTYPE_F16 && dtype != QI21_DTYPE_BF16) return fail(QI21_ERR_ARG, "dtype %d", dtype);
+  return QI21_OK;
+}
+
+int qi21_op_rowop(int32_t dtype, int32_t rows, int32_t dim, float eps, float* x, const float* y, const float* gate_t,
                   const float* scale, void* xn, void* stream) {
+  if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
   if (rows < 0 || dim <= 0 || dim % 4 || dim > 8192) return fail(QI21_ERR_SHAPE, "rows %d dim %d", rows, dim);
   if (rows == 0) return QI21_OK;  // empty input: nothing to do
   if (x == nullptr || (y && !gate_t) || (xn && !scale) || (!y && !xn)) return fail(QI21_ERR_ARG, "null pointer");
-  QI21_CK(launch_rowop(rows, dim, eps, x, y, gate_t, scale, static_cast<__half*>(xn),
-                       static_cast<cudaStream_t>(stream)),
-          "rowop");
+  QI21_CK(launch_rowop(rows, dim, eps, x, y, gate_t, scale, xn, dtype, static_cast<cudaStream_t>(stream)), "rowop");
   return QI21_OK;
 }
 
@@ -1127,8 +1210,9 @@ int qi21_op_mods_prep(int32_t dim, const float* mods, float* md, void* stream) {
   return QI21_OK;
 }
 
-int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* out,
-                 int32_t ldo, const float* gate_t, void* stream) {
+int qi21_op_gemm(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B,
+                 void* out, int32_t ldo, const float* gate_t, void* stream) {
+  if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
   if (epi < 0 || epi > 3) return fail(QI21_ERR_ARG, "epilogue %d", epi);
   if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 64) return fail(QI21_ERR_SHAPE, "M %d N %d K %d", M, N, K);
   if (M == 0) return QI21_OK;
@@ -1139,9 +1223,7 @@ int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, co
     return fail(QI21_ERR_ARG, "A, B and out must be 16-byte aligned");
   if (M == 0) return QI21_OK;
   GemmPlan p;
-  QI21_CK(make_gemm_plan(&p, epi, M, N, K, static_cast<const __half*>(A), static_cast<const __half*>(B), out,
-                         ldo, gate_t),
-          "gemm plan");
+  QI21_CK(make_gemm_plan(&p, epi, dtype, M, N, K, A, B, out, ldo, gate_t), "gemm plan");
   QI21_CK(launch_gemm(p, static_cast<cudaStream_t>(stream)), "gemm");
   return QI21_OK;
 }
@@ -1187,16 +1269,16 @@ int qi21_op_gemm_fp8(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A
   return QI21_OK;
 }
 
-int qi21_op_qkrope(int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
+int qi21_op_qkrope(int32_t dtype, int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
                    const float* norm_k, const float* cos_, const float* sin_, void* stream) {
+  if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
   if (rows < 0 || heads <= 0) return fail(QI21_ERR_SHAPE, "rows %d heads %d", rows, heads);
   if (rows == 0) return QI21_OK;
   if (!panel || !norm_q || !norm_k || !cos_ || !sin_) return fail(QI21_ERR_ARG, "null pointer");
   RopeTables t{};
   t.nsrc = 1;
   t.src[0] = RopeSrc{cos_, sin_, 0};
-  QI21_CK(launch_qkrope(rows, heads, eps, static_cast<__half*>(panel), norm_q, norm_k, t,
-                        static_cast<cudaStream_t>(stream)),
+  QI21_CK(launch_qkrope(rows, heads, eps, panel, dtype, norm_q, norm_k, t, static_cast<cudaStream_t>(stream)),
           "qkrope");
   return QI21_OK;
 }
@@ -1205,25 +1287,25 @@ int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void*
   if (rows < 0 || dim <= 0 || dim % 8) return fail(QI21_ERR_SHAPE, "rows %d dim %d", rows, dim);
   if (rows == 0) return QI21_OK;
   if (!panel || !kv) return fail(QI21_ERR_ARG, "null pointer");
-  QI21_CK(launch_kvcopy(rows, dim, static_cast<const __half*>(panel), static_cast<__half*>(kv),
-                        static_cast<cudaStream_t>(stream)),
-          "kvcopy");
+  QI21_CK(launch_kvcopy(rows, dim, panel, kv, static_cast<cudaStream_t>(stream)), "kvcopy");
   return QI21_OK;
 }
 
-int qi21_op_attention(int32_t nq, int32_t heads, const void* panel, const void* kv_pre, int32_t n_pre,
+int qi21_op_attention(int32_t dtype, int32_t nq, int32_t heads, const void* panel, const void* kv_pre, int32_t n_pre,
                       int32_t n_own, const uint32_t* vis, void* out, void* stream) {
+  if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
   if (nq < 0 || heads <= 0 || n_pre < 0 || n_own < 0) return fail(QI21_ERR_SHAPE, "bad sizes");
   if (nq > n_own) return fail(QI21_ERR_SHAPE, "nq %d > own rows %d (queries are panel rows)", nq, n_own);
   if (nq == 0) return QI21_OK;
   if (!panel || !out || (n_pre > 0 && !kv_pre)) return fail(QI21_ERR_ARG, "null pointer");
   AttnArgs a{};
-  a.panel = static_cast<const __half*>(panel);
+  a.panel = panel;
   a.panel_rows = n_own;
-  a.out = static_cast<__half*>(out);
+  a.out = out;
   a.heads = heads;
+  a.dt = dtype;
   a.nseq = 1;
-  a.seq[0] = AttnSeq{static_cast<const __half*>(kv_pre), n_pre, 0, nq, 0, n_own, vis};
+  a.seq[0] = AttnSeq{kv_pre, n_pre, 0, nq, 0, n_own, vis};
   QI21_CK(launch_attention(a, static_cast<cudaStream_t>(stream)), "attention");
   return QI21_OK;
 }

@@ -3,20 +3,50 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace qi21 {
+
+// 16-bit element type of the weight planes, the activation rows (xn, qkv
+// panel, attention output, SwiGLU hidden rows) and the K/V cache; the
+// residual stream is f32 either way (qi21_geom::dtype).
+enum Dt : int { DT_F16 = 0, DT_BF16 = 1 };
+
+// One-time set-up kept per CUDA device (kernel attributes, the SM count):
+// the runtime applies function attributes per device, so a process that
+// drives several devices initialises each on its first call there.
+constexpr int kMaxDevices = 64;
+template <class T>
+class PerDevice {
+ public:
+  // The value of the current device, made by make() on its first use there
+  // (thread-safe); nullptr if there is no usable current device.
+  template <class F>
+  const T* get(F&& make) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(once_[dev], [&] { val_[dev] = make(); });
+    return &val_[dev];
+  }
+
+ private:
+  std::once_flag once_[kMaxDevices];
+  T val_[kMaxDevices] = {};
+};
 
 // ------------------------------------------------------------ row kernels --
 
 // md = [s1 | tanh g1 | s2 | tanh g2]
 cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t s);
 
-// if y: x += gate_t * y; if xn: xn = f16(LN(x)(1 + scale))
+// if y: x += gate_t * y; if xn: xn = dt(LN(x)(1 + scale))
 cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y,
-                         const float* gate_t, const float* scale, __half* xn, cudaStream_t s);
+                         const float* gate_t, const float* scale, void* xn, int dt, cudaStream_t s);
 
 // Per-row RoPE table source: rows [row0, row0 + rows) use cos/sin + (r - row0)*64.
 struct RopeSrc {
@@ -30,15 +60,16 @@ struct RopeTables {
   RopeSrc src[kMaxSeq];
 };
 
-// In place on panel f16 [rows][3H]: q, k RMSNorm * w then interleaved RoPE.
-cudaError_t launch_qkrope(int rows, int heads, float eps, __half* panel, const float* norm_q,
+// In place on panel dt [rows][3H]: q, k RMSNorm * w then interleaved RoPE.
+cudaError_t launch_qkrope(int rows, int heads, float eps, void* panel, int dt, const float* norm_q,
                           const float* norm_k, const RopeTables& tabs, cudaStream_t s);
 
-// kv f16 [rows][2H] = panel[:, H:3H]
-cudaError_t launch_kvcopy(int rows, int dim, const __half* panel, __half* kv, cudaStream_t s);
+// kv [rows][2H] = panel[:, H:3H] (16-bit elements)
+cudaError_t launch_kvcopy(int rows, int dim, const void* panel, void* kv, cudaStream_t s);
 
-// w13 interleave: dst [2I][H] from gate [I][H], up [I][H], 64-row blocks.
-cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half* up, __half* dst,
+// w13 interleave: dst [2I][H] from gate [I][H], up [I][H], 64-row blocks
+// (16-bit elements).
+cudaError_t launch_pack_w13(int inter, int dim, const void* gate, const void* up, void* dst,
                             cudaStream_t s);
 
 // x[n][dim] = tok[n][64] w_in[dim][64]^T (f32)
@@ -53,8 +84,8 @@ cudaError_t launch_quant_rows(int rows, int cols, const __half* a, size_t lda, u
 cudaError_t launch_timestep(int dim, float t, const float* t_lin1, const float* t_lin2, const float* modulation,
                             const float* norm_out, float* work, float* mods, float* final_scale, cudaStream_t s);
 // Synchronous: zeroes the counter, scans on s, reads it back, syncs s.
-// elem_bytes 4 (f32) or 2 (f16); x aligned to elem_bytes.
-cudaError_t count_nonfinite(const void* x, size_t count, int elem_bytes, unsigned long long* out, cudaStream_t s);
+// elem: 4 (f32), 2 (f16) or 3 (bf16, 2 bytes); x aligned to its element.
+cudaError_t count_nonfinite(const void* x, size_t count, int elem, unsigned long long* out, cudaStream_t s);
 cudaError_t launch_final(int n, int dim, float eps, const float* x, const float* fs, const float* w_out,
                          float* out, cudaStream_t s);
 
@@ -73,11 +104,12 @@ struct QkvEpi {
 };
 
 struct GemmPlan {
-  CUtensorMap tmA;  // A f16 [M][K], box 64 x 128, 128B swizzle
-  CUtensorMap tmB;  // B f16 [N][K], box 64 x BN, 128B swizzle
-  CUtensorMap tmBh; // B f16 [N][K], box 64 x BN/2 (split tiles of a partial last wave)
+  CUtensorMap tmA;  // A dt [M][K], box 64 x 128, 128B swizzle
+  CUtensorMap tmB;  // B dt [N][K], box 64 x BN, 128B swizzle
+  CUtensorMap tmBh; // B dt [N][K], box 64 x BN/2 (split tiles of a partial last wave)
   CUtensorMap tmX;  // EPI_RESID: x f32 [M][ldo], box 32 x 32, 128B swizzle
   int M, N, K, bn, epi, ldo;
+  int dt;            // operand and 16-bit output type (f16 path); DT_F16 for FP8
   void* out;
   const float* gate;
   QkvEpi qkv;
@@ -86,9 +118,10 @@ struct GemmPlan {
   const float* sw;   // FP8: per B row scale
 };
 
-// Encode the tensor maps of C = A B^T. Returns cudaSuccess or an error.
-cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
-                           const __half* B, void* out, int ldo, const float* gate);
+// Encode the tensor maps of C = A B^T with A, B of type dt. Returns
+// cudaSuccess or an error; launches nothing.
+cudaError_t make_gemm_plan(GemmPlan* p, int epi, int dt, int M, int N, int K, const void* A,
+                           const void* B, void* out, int ldo, const float* gate);
 // The FP8 form: A, B E4M3 codes [M][K], [N][K] (row pitch K bytes), the
 // accumulator scaled by sa[row] sw[col]; N % 256 == 0, K % 128 == 0.
 cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const uint8_t* A, const float* sa,
@@ -98,7 +131,7 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s);
 // -------------------------------------------------------------- attention --
 
 struct AttnSeq {
-  const __half* kv_pre;  // [n_pre][2H] K then V, or null
+  const void* kv_pre;  // [n_pre][2H] K then V (dt), or null
   int n_pre;
   int q_row0;    // first query row in the panel / output
   int nq;        // query rows
@@ -108,14 +141,40 @@ struct AttnSeq {
 };
 
 struct AttnArgs {
-  const __half* panel;  // [panel_rows][3H]: q at 0, k at H, v at 2H
+  const void* panel;  // [panel_rows][3H] dt: q at 0, k at H, v at 2H
   int panel_rows;
-  __half* out;          // [.][H]
+  void* out;          // [.][H] dt
   int heads;
+  int dt;
   int nseq;
   AttnSeq seq[kMaxSeq];
 };
 
+// Kernel parameters of one attention launch (tensor maps encoded).
+struct AttnTcSeq {
+  CUtensorMap kvmap;  // cache [n_pre][2H], box 64 x 64 (unused if n_pre == 0)
+  const uint32_t* vis;
+  int n_pre, pad_end, q_row0, nq, own_row0, n_own;
+};
+
+struct AttnTcParams {
+  CUtensorMap panel;     // [rows][3H], box 64 x 128 (Q)
+  CUtensorMap panel_kv;  // same, box 64 x 64 (K, V)
+  void* out;
+  int H;
+  float scale_log2;
+  AttnTcSeq seq[kMaxSeq];
+};
+
+struct AttnPlan {
+  AttnTcParams prm;
+  int dt;
+  int gx, gy, gz;  // grid; gx == 0: nothing to launch
+};
+
+// Encode the maps of an attention launch (launches nothing), then launch.
+cudaError_t make_attn_plan(const AttnArgs& a, AttnPlan* p);
+cudaError_t launch_attn_plan(const AttnPlan& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 
 // --------------------------------------------------------------- device ----

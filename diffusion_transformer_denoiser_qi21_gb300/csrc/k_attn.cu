@@ -1,6 +1,8 @@
 // Flash attention over [prefix cache, own panel rows] with a leading-run
 // visibility mask, on the 5th-generation tensor cores (qwen_image21.rs,
-// Qi21Dit::attention + softmax_prefix; gpu_wgpu/qi21.rs, qi_flash).
+// Qi21Dit::attention + softmax_prefix; gpu_wgpu/qi21.rs, qi_flash). Q, K,
+// V, P and the output are f16, or bf16 in the bf16 instance (BF), with f32
+// scores, softmax and accumulation either way.
 //
 // Query i of a sequence sees keys [0, lim(i)), lim(i) = min(vis[i], keys)
 // in the prefill (block-causal) and every key in a step. Keys j < n_pre
@@ -70,21 +72,6 @@ constexpr int kAttnSmem = kOffX + 1024 + 1024;
 constexpr int kAttnThreads = 320;           // 10 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 in f16
 
-struct AttnTcSeq {
-  CUtensorMap kvmap;  // cache [n_pre][2H] f16, box 64 x 64 (unused if n_pre == 0)
-  const uint32_t* vis;
-  int n_pre, pad_end, q_row0, nq, own_row0, n_own;
-};
-
-struct AttnTcParams {
-  CUtensorMap panel;     // [rows][3H] f16, box 64 x 128 (Q)
-  CUtensorMap panel_kv;  // same, box 64 x 64 (K, V)
-  __half* out;
-  int H;
-  float scale_log2;
-  AttnTcSeq seq[kMaxSeq];
-};
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -139,6 +126,7 @@ __device__ __forceinline__ int key_index(int v, int n_pre, int pad_end) {
   return v < n_pre ? v : (v >= pad_end ? v - pad_end + n_pre : 0x7fffffff);
 }
 
+template <bool BF>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -243,8 +231,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(128, kAK, false);
-      constexpr uint32_t idesc_pv = idesc_f16(128, 128, true);  // V: MN-major
+      constexpr uint32_t idesc_qk = idesc_f16(128, kAK, false, BF);
+      constexpr uint32_t idesc_pv = idesc_f16(128, 128, true, BF);  // V: MN-major
       const uint32_t sQ = smem_u32(smem + kOffQ);
       bool ok = mbar_wait(qfull, 0, abort_flag, &s_attn_status);
       auto issue_qk = [&](int j) -> bool {
@@ -372,7 +360,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
           break;
         }
       }
-      // this half of the P row -> TMEM: 96 keys = 48 columns of f16 pairs
+      // this half of the P row -> TMEM: 96 keys = 48 columns of 16-bit pairs
       // (32 + 16) over S_b
       const uint64_t nm2 = f2(-m, -m);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -389,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
           unf2(x, x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
           acc[i & 3] = fadd2(acc[i & 3], f2(p0, p1));
-          pk[i] = pack_half2(p0, p1);
+          pk[i] = pack2<BF>(p0, p1);
         }
         if (part == 0)
           tmem_st32(tP + b * kAK + hf * (kHalf / 2) + lane_off, pk);
@@ -428,7 +416,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       xch[hf * 128 + r] = l;
       pair_sync();
       const float inv = 1.f / (l + xch[(hf ^ 1) * 128 + r]);
-      __half* orow = p.out + static_cast<size_t>(sq.q_row0 + qi) * H + h * kAD + hf * 64;
+      uint16_t* orow = static_cast<uint16_t*>(p.out) + static_cast<size_t>(sq.q_row0 + qi) * H + h * kAD + hf * 64;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[32];
@@ -439,10 +427,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             dst[g] = make_uint4(
-                pack_half2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv),
-                pack_half2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv),
-                pack_half2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv),
-                pack_half2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv));
+                pack2<BF>(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv),
+                pack2<BF>(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv),
+                pack2<BF>(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv),
+                pack2<BF>(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv));
         }
       }
     }
@@ -472,17 +460,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
   return fn;
 }
 
-static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                               int dt) {
   auto fn = attn_encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
+  const CUtensorMapDataType type = dt == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   auto encode = [&] {
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return fn(m, type, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   CUresult r = encode();
   // a host thread whose first library call this is may have no context yet
@@ -490,18 +479,18 @@ static cudaError_t encode_rows(CUtensorMap* m, const void* ptr, uint64_t cols, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-  if (attr != cudaSuccess) return attr;
-  AttnTcParams prm;
-  memset(&prm, 0, sizeof prm);
+cudaError_t make_attn_plan(const AttnArgs& in, AttnPlan* p) {
+  if (in.dt != DT_F16 && in.dt != DT_BF16) return cudaErrorInvalidValue;
+  memset(p, 0, sizeof *p);
+  AttnTcParams& prm = p->prm;
   const int H = in.heads * kAD;
+  p->dt = in.dt;
   prm.out = in.out;
   prm.H = H;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kAD)));
-  cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAQ);
-  if (e == cudaSuccess) e = encode_rows(&prm.panel_kv, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kKVBox);
+  cudaError_t e = encode_rows(&prm.panel, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kAQ, in.dt);
+  if (e == cudaSuccess)
+    e = encode_rows(&prm.panel_kv, in.panel, static_cast<uint64_t>(3) * H, in.panel_rows, kKVBox, in.dt);
   if (e != cudaSuccess) return e;
   int maxq = 0;
   for (int i = 0; i < in.nseq; ++i) {
@@ -515,15 +504,39 @@ cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
     t.own_row0 = a.own_row0;
     t.n_own = a.n_own;
     if (a.n_pre > 0) {
-      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre, kKVBox);
+      e = encode_rows(&t.kvmap, a.kv_pre, static_cast<uint64_t>(2) * H, a.n_pre, kKVBox, in.dt);
       if (e != cudaSuccess) return e;
     }
     maxq = std::max(maxq, a.nq);
   }
-  if (maxq == 0) return cudaSuccess;
-  dim3 grid((maxq + kAQ - 1) / kAQ, in.heads, in.nseq);
-  attn_tc_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(prm);
+  p->gx = (maxq + kAQ - 1) / kAQ;
+  p->gy = in.heads;
+  p->gz = in.nseq;
+  return cudaSuccess;
+}
+
+template <bool BF>
+static cudaError_t launch_attn_t(const AttnPlan& p, cudaStream_t s) {
+  // shared-memory opt-in, once per instance and device
+  static PerDevice<cudaError_t> once;
+  const cudaError_t* attr = once.get(
+      [] { return cudaFuncSetAttribute(attn_tc_kernel<BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem); });
+  if (attr == nullptr) return cudaErrorNoDevice;
+  if (*attr != cudaSuccess) return *attr;
+  attn_tc_kernel<BF><<<dim3(p.gx, p.gy, p.gz), kAttnThreads, kAttnSmem, s>>>(p.prm);
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_plan(const AttnPlan& p, cudaStream_t s) {
+  if (p.gx == 0) return cudaSuccess;
+  return p.dt == DT_BF16 ? launch_attn_t<true>(p, s) : launch_attn_t<false>(p, s);
+}
+
+cudaError_t launch_attention(const AttnArgs& in, cudaStream_t s) {
+  AttnPlan p;
+  const cudaError_t e = make_attn_plan(in, &p);
+  if (e != cudaSuccess) return e;
+  return launch_attn_plan(p, s);
 }
 
 }  // namespace qi21

@@ -1,6 +1,7 @@
-// tcgen05 GEMM for the block's four projections: C = A B^T with A f16
-// [M][K] (activations) and B f16 [N][K] (nn.Linear weights), both K-major,
-// f32 accumulation in TMEM, fused epilogues:
+// tcgen05 GEMM for the block's four projections: C = A B^T with A [M][K]
+// (activations) and B [N][K] (nn.Linear weights), both K-major and both f16
+// or both bf16 (the geometry's dtype), f32 accumulation in TMEM, fused
+// epilogues whose 16-bit outputs take the same type:
 //   EPI_F16    qkv panel store                (gpu_wgpu/qi21.rs, zi_mm f16)
 //   EPI_RESID  x += tanh(g) * acc on the f32 residual stream (the O and down
 //              projections followed by Qi21Dit::gated_add); x moves through
@@ -14,7 +15,7 @@
 //              whole 128-column head vectors of its row)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
-// The FP8 instance (F8 = true) runs the same pipeline on E4M3 operands:
+// The FP8 instance (OP = kOpF8) runs the same pipeline on E4M3 operands:
 // byte-wide tensor maps with 128-byte boxes (128 elements per k-block, the
 // same swizzled 128-byte rows), tcgen05.mma.kind::f8f6f4 (K = 32), and the
 // accumulator multiplied by the A row scale and the B row (output channel)
@@ -30,6 +31,9 @@
 //   warp 0     TMA producer (both CTAs): A 128x64 and B (BN/2)x64 tiles
 //              (128-byte swizzle) into a 6-stage ring; the loads of both CTAs
 //              complete on the even CTA's "full" mbarrier
+// Tiles are visited in groups of G pair rows (column blocks outer, the
+// pair rows of a group inner), G chosen on the host so that the group's A
+// rows stay in L2 while its column blocks stream past.
 //   warp 1     TMEM allocation (jointly, both CTAs); in the even CTA one
 //              thread issues the pair MMAs (M=256, N=BN, K=16) and commits
 //              that release a stage / publish an accumulator in both CTAs
@@ -60,6 +64,13 @@ unsigned int gemm_status_read_clear() {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
+// Operand kinds of an instance: f16 or bf16 A/B (kind::f16, 16-bit
+// epilogue outputs of the same type) or E4M3 codes (kind::f8f6f4, f16
+// epilogue outputs).
+constexpr int kOpF16 = 0;
+constexpr int kOpBF16 = 1;
+constexpr int kOpF8 = 2;
+
 
 template <int BN, int EPI>
 struct GemmCfg {
@@ -89,9 +100,9 @@ struct EpiArgs {
 };
 
 // FP8: 32 accumulator columns starting at column `col` times sa sw[col + i]
-template <bool F8>
+template <int OP>
 __device__ __forceinline__ void f8_scale(uint32_t (&r)[32], float sa, const float* __restrict__ sw, int col) {
-  if constexpr (F8) {
+  if constexpr (OP == kOpF8) {
     const float4* s4 = reinterpret_cast<const float4*>(sw + col);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -106,13 +117,15 @@ __device__ __forceinline__ void f8_scale(uint32_t (&r)[32], float sa, const floa
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
 
-template <int BN, int EPI, bool F8>
+template <int BN, int EPI, int OP>
 __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0, int bn,
                                               const EpiArgs& ep) {
+  constexpr bool F8 = OP == kOpF8;
+  constexpr bool BF = OP == kOpBF16;  // 16-bit outputs in bf16
   const bool live = row < M;
   const float sa = (F8 && live) ? ep.sa[row] : 1.f;
   if constexpr (EPI == EPI_SWIGLU) {
-    __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
+    uint16_t* out = static_cast<uint16_t*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
 #pragma unroll 1
     for (int p = 0; p < bn / 128; ++p) {
 #pragma unroll 1
@@ -122,8 +135,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
         tmem_ld32(tbase + p * 128 + 64 + c * 32, u);
         tmem_ld_wait(g);
         tmem_ld_wait(u);
-        f8_scale<F8>(g, sa, ep.sw, n0 + p * 128 + c * 32);
-        f8_scale<F8>(u, sa, ep.sw, n0 + p * 128 + 64 + c * 32);
+        f8_scale<OP>(g, sa, ep.sw, n0 + p * 128 + c * 32);
+        f8_scale<OP>(u, sa, ep.sw, n0 + p * 128 + 64 + c * 32);
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(out + p * 64 + c * 32);
 #pragma unroll
@@ -134,7 +147,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
               const int i = 8 * j + 2 * e;
               const float h0 = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
               const float h1 = silu_f(__uint_as_float(g[i + 1])) * __uint_as_float(u[i + 1]);
-              w[e] = pack_half2(h0, h1);
+              w[e] = pack2<BF>(h0, h1);
             }
             dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
           }
@@ -143,7 +156,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     }
   } else if constexpr (EPI == EPI_QKV) {
     const QkvEpi& qe = ep.qkv;
-    __half* out = static_cast<__half*>(ep.out) + static_cast<size_t>(row) * ep.ldo;
+    uint16_t* out = static_cast<uint16_t*>(ep.out) + static_cast<size_t>(row) * ep.ldo;
     // this row's RoPE table (the sequence whose rows contain it)
     int si = 0;
 #pragma unroll
@@ -163,7 +176,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
       for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
       if (!live) continue;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) f8_scale<F8>(r[c], sa, ep.sw, col + c * 32);
+      for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
       uint4* dst = reinterpret_cast<uint4*>(out + col);
       if (part == 2) {
 #pragma unroll
@@ -171,10 +184,10 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             dst[c * 4 + j] = make_uint4(
-                pack_half2(__uint_as_float(r[c][8 * j + 0]), __uint_as_float(r[c][8 * j + 1])),
-                pack_half2(__uint_as_float(r[c][8 * j + 2]), __uint_as_float(r[c][8 * j + 3])),
-                pack_half2(__uint_as_float(r[c][8 * j + 4]), __uint_as_float(r[c][8 * j + 5])),
-                pack_half2(__uint_as_float(r[c][8 * j + 6]), __uint_as_float(r[c][8 * j + 7])));
+                pack2<BF>(__uint_as_float(r[c][8 * j + 0]), __uint_as_float(r[c][8 * j + 1])),
+                pack2<BF>(__uint_as_float(r[c][8 * j + 2]), __uint_as_float(r[c][8 * j + 3])),
+                pack2<BF>(__uint_as_float(r[c][8 * j + 4]), __uint_as_float(r[c][8 * j + 5])),
+                pack2<BF>(__uint_as_float(r[c][8 * j + 6]), __uint_as_float(r[c][8 * j + 7])));
         continue;
       }
       float ss[4] = {0.f, 0.f, 0.f, 0.f};
@@ -204,10 +217,10 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
           const float b2 = __uint_as_float(r[c][8 * j + 5]) * inv * wb.y;
           const float a3 = __uint_as_float(r[c][8 * j + 6]) * inv * wb.z;
           const float b3 = __uint_as_float(r[c][8 * j + 7]) * inv * wb.w;
-          dst[c * 4 + j] = make_uint4(pack_half2(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
-                                      pack_half2(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
-                                      pack_half2(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
-                                      pack_half2(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
+          dst[c * 4 + j] = make_uint4(pack2<BF>(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
+                                      pack2<BF>(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
+                                      pack2<BF>(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
+                                      pack2<BF>(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
         }
       }
     }
@@ -219,16 +232,16 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
       tmem_ld_wait(r);
       if (!live) continue;
       const int col = n0 + c * 32;
-      f8_scale<F8>(r, sa, ep.sw, col);
+      f8_scale<OP>(r, sa, ep.sw, col);
       if constexpr (EPI == EPI_F16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(ep.out) +
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ep.out) +
                                               static_cast<size_t>(row) * ep.ldo + col);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          dst[j] = make_uint4(pack_half2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
-                              pack_half2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                              pack_half2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                              pack_half2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+          dst[j] = make_uint4(pack2<BF>(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                              pack2<BF>(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                              pack2<BF>(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                              pack2<BF>(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
         }
       } else if constexpr (EPI == EPI_F32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) +
@@ -258,27 +271,47 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 
 // Tile pair t of the persistent schedule (one pair per cluster step): the
 // first nfull pairs are 2 x (BM x BN) with pair row mp (tile rows 2 mp and
-// 2 mp + 1) and column block n; when the last wave would be at most half
+// 2 mp + 1) and column block nb; when the last wave would be at most half
 // full, its pairs are split into two halves of BN/2 columns (same K order
 // per output element, so identical results) that fill one half-length wave.
+// Full tile f lies in group f / (G nN) of G pair rows (the last group may
+// be smaller); inside a group the pair rows run fastest, then the column
+// blocks, so the clusters of a wave work on a band of about G pair rows and
+// a few column blocks, and the group's A rows are reused from L2 across its
+// column blocks. G = num_mp is plain pair-rows-fastest order.
 struct TileInfo {
   int mp, n0, bn;
 };
 
-template <int BN>
-__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nfull) {
-  if (t < nfull) return TileInfo{t % num_mp, (t / num_mp) * BN, BN};
-  const int u = t - nfull;
-  const int tf = nfull + (u >> 1);
-  return TileInfo{tf % num_mp, (tf / num_mp) * BN + (u & 1) * (BN / 2), BN / 2};
+__device__ __forceinline__ void raster(int f, int num_mp, int nN, int G, int& mp, int& nb) {
+  const int per_group = G * nN;
+  const int g = f / per_group;
+  const int first = g * G;
+  const int gs = min(G, num_mp - first);
+  const int r = f - g * per_group;
+  mp = first + r % gs;
+  nb = r / gs;
 }
 
-template <int BN, int EPI, bool F8>
+template <int BN>
+__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, int nfull) {
+  int mp, nb;
+  if (t < nfull) {
+    raster(t, num_mp, nN, G, mp, nb);
+    return TileInfo{mp, nb * BN, BN};
+  }
+  const int u = t - nfull;
+  raster(nfull + (u >> 1), num_mp, nN, G, mp, nb);
+  return TileInfo{mp, nb * BN + (u & 1) * (BN / 2), BN / 2};
+}
+
+template <int BN, int EPI, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmX, int M,
-                   int N, int K, int nfull, int num_tiles, EpiArgs ep) {
+                   int N, int K, int group, int nfull, int num_tiles, EpiArgs ep) {
   using C = GemmCfg<BN, EPI>;
+  constexpr bool F8 = OP == kOpF8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -297,6 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
   const int num_mp = ((M + kBM - 1) / kBM + 1) / 2;
+  const int nN = N / BN;
   constexpr int kKE = F8 ? 128 : kBK;  // K elements per k-block (128 bytes per row)
   const int nk = K / kKE;
 
@@ -334,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-        const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
+        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull);
         const bool half = ti.bn != BN;
         const int m0 = (2 * ti.mp + rank) * kBM;
         const int bh = ti.bn / 2;  // B rows this CTA holds
@@ -359,8 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc_full = idesc_f16(2 * kBM, BN);
-      constexpr uint32_t idesc_half = idesc_f16(2 * kBM, BN / 2);
+      constexpr uint32_t idesc_full = idesc_f16(2 * kBM, BN, false, OP == kOpBF16);
+      constexpr uint32_t idesc_half = idesc_f16(2 * kBM, BN / 2, false, OP == kOpBF16);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
@@ -403,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     int xu = 0;  // EPI_RESID: x chunks this warp has used (buffer xu & 1)
     bool eok = true;
     for (int t = cluster; t < num_tiles && eok; t += nclusters, ++it) {
-      const TileInfo ti = tile_at<BN>(t, num_mp, nfull);
+      const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
@@ -420,6 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int row = row0 + lane;
         const float sa = (F8 && row < M) ? ep.sa[row] : 1.f;
         const int nch = ti.bn / 32;
+        int issued = 0;  // x chunks of this tile whose loads were issued
         auto load = [&](int c) {
           if (lane == 0) {
             const int b = (xu + c) % NB;
@@ -427,10 +462,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             mbar_arrive_expect_tx(&xb[b], 4096);
             tma_load_2d(eb + b * 4096, &tmX, &xb[b], ti.n0 + 32 * c, row0);
           }
+          issued = c + 1;
         };
         for (int c = 0; c < NB - 1 && c < nch; ++c) load(c);
         for (int c = 0; c < nch; ++c) {
-          if (c + NB - 1 < nch) load(c + NB - 1);
+          if (c + NB - 1 < nch && !*abort_flag) load(c + NB - 1);
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           const int u = xu + c;
@@ -438,10 +474,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
               mbar_wait(&xb[u % NB], static_cast<uint32_t>(u / NB) & 1u, abort_flag, &s_gemm_status);
           tmem_ld_wait(r);
           if (!got) {
+            // another role gave up: let the x loads this warp issued land
+            // before the CTA leaves (their bytes target this CTA's buffers)
+            if (lane == 0)
+              for (int d = c; d < issued; ++d)
+                mbar_wait_drain(&xb[(xu + d) % NB], static_cast<uint32_t>((xu + d) / NB) & 1u);
+            __syncwarp();
             eok = false;
             break;
           }
-          f8_scale<F8>(r, sa, ep.sw, ti.n0 + 32 * c);
+          f8_scale<OP>(r, sa, ep.sw, ti.n0 + 32 * c);
           float4* xs = reinterpret_cast<float4*>(eb + (u % NB) * 4096 + lane * 128);
           const float4* g4 = reinterpret_cast<const float4*>(ep.gate + ti.n0 + 32 * c);
 #pragma unroll
@@ -464,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         xu += nch;
       } else {
-        gemm_epilogue<BN, EPI, F8>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
+        gemm_epilogue<BN, EPI, OP>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
       }
       tc_fence_before();
       __syncwarp();
@@ -499,11 +541,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D f16 (or byte) tensor [outer][inner] with the given row pitch; box
-// inner x outer.
-static cudaError_t encode_f16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                                 bool bytes = false, bool f32 = false) {
+// Element types of the tensor maps.
+enum MapType { MAP_F16, MAP_BF16, MAP_U8, MAP_F32 };
+
+// 2-D tensor [outer][inner] of `type` with the given row pitch; box
+// inner x outer, 128-byte swizzle.
+static cudaError_t encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, MapType type) {
   auto fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {inner, outer};
@@ -511,11 +555,11 @@ static cudaError_t encode_f16_2d(CUtensorMap* m, const void* ptr, uint64_t inner
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   auto encode = [&] {
-    return fn(m,
-              f32     ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-              : bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-              2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt = type == MAP_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : type == MAP_U8   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : type == MAP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   CUresult r = encode();
@@ -531,15 +575,18 @@ static cudaError_t encode_x_map(GemmPlan* p) {
     p->tmX = p->tmA;
     return cudaSuccess;
   }
-  return encode_f16_2d(&p->tmX, p->out, p->N, p->M, static_cast<uint64_t>(p->ldo) * 4, 32, 32, false, true);
+  return encode_2d(&p->tmX, p->out, p->N, p->M, static_cast<uint64_t>(p->ldo) * 4, 32, 32, MAP_F32);
 }
 
-cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __half* A,
-                           const __half* B, void* out, int ldo, const float* gate) {
+cudaError_t make_gemm_plan(GemmPlan* p, int epi, int dt, int M, int N, int K, const void* A, const void* B,
+                           void* out, int ldo, const float* gate) {
+  if (dt != DT_F16 && dt != DT_BF16) return cudaErrorInvalidValue;
+  const MapType mt = dt == DT_BF16 ? MAP_BF16 : MAP_F16;
   p->M = M;
   p->N = N;
   p->K = K;
   p->epi = epi;
+  p->dt = dt;
   p->ldo = ldo;
   p->out = out;
   p->gate = gate;
@@ -547,13 +594,13 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int M, int N, int K, const __ha
   p->f8 = false;
   p->sa = p->sw = nullptr;
   p->bn = (N % 256 == 0) ? 256 : 128;
-  cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM);
+  cudaError_t e = encode_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, mt);
   if (e != cudaSuccess) return e;
   // each CTA of a cluster loads half of the B tile (and a quarter in the
   // split tail)
-  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2);
+  e = encode_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2, mt);
   if (e != cudaSuccess) return e;
-  e = encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4);
+  e = encode_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4, mt);
   if (e != cudaSuccess) return e;
   return encode_x_map(p);
 }
@@ -564,6 +611,7 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
   p->N = N;
   p->K = K;
   p->epi = epi;
+  p->dt = DT_F16;
   p->ldo = ldo;
   p->out = out;
   p->gate = gate;
@@ -572,26 +620,38 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
   p->sa = sa;
   p->sw = sw;
   p->bn = 256;
-  cudaError_t e = encode_f16_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K), 128, kBM, true);
+  cudaError_t e = encode_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K), 128, kBM, MAP_U8);
   if (e != cudaSuccess) return e;
-  e = encode_f16_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 2, true);
+  e = encode_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 2, MAP_U8);
   if (e != cudaSuccess) return e;
-  e = encode_f16_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, true);
+  e = encode_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, MAP_U8);
   if (e != cudaSuccess) return e;
   return encode_x_map(p);
 }
 
-template <int BN, int EPI, bool F8 = false>
+// Pair rows per raster group: all of them while the whole A operand fits
+// comfortably in L2, else as many as keep the group's A rows within
+// kGroupBytes (the rest of L2 holds the streamed B column blocks).
+constexpr size_t kGroupBytes = 56ull << 20;
+
+static int raster_group(int num_mp, int K, int elem_bytes) {
+  const size_t pair_bytes = static_cast<size_t>(2 * kBM) * K * elem_bytes;
+  const size_t g = std::max<size_t>(1, kGroupBytes / pair_bytes);
+  return static_cast<int>(std::min<size_t>(g, static_cast<size_t>(num_mp)));
+}
+
+template <int BN, int EPI, int OP = kOpF16>
 static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   using C = GemmCfg<BN, EPI>;
   // shared-memory opt-in and the resident cluster count, once per
-  // instance, thread-safely, on first use
+  // instance and device, thread-safely, on first use there
   struct Init {
     cudaError_t e;
     int clusters;
   };
-  static const Init init = [] {
-    Init r{cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDevice<Init> once;
+  const Init* init = once.get([] {
+    Init r{cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmem),
            1};
     if (r.e != cudaSuccess) return r;
@@ -600,12 +660,13 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     int n = 0;
-    r.e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, F8>, &cfg);
+    r.e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, OP>, &cfg);
     r.clusters = n > 0 ? n : 1;
     return r;
-  }();
-  if (init.e != cudaSuccess) return init.e;
-  const int max_clusters = init.clusters;
+  });
+  if (init == nullptr) return cudaErrorNoDevice;
+  if (init->e != cudaSuccess) return init->e;
+  const int max_clusters = init->clusters;
   const int num_mp = ((p.M + kBM - 1) / kBM + 1) / 2;
   const int pairs = num_mp * (p.N / BN);
   // split the pairs of a partial last wave that is at most half full
@@ -616,10 +677,33 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     total = nfull + 2 * rem;
   }
   const int clusters = std::min(total, max_clusters);
+  const int group = raster_group(num_mp, p.K, OP == kOpF8 ? 1 : 2);
   EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw};
-  gemm_tc_kernel<BN, EPI, F8><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.tmX, p.M, p.N, p.K,
-                                                                   nfull, total, ep);
+  gemm_tc_kernel<BN, EPI, OP><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.tmX, p.M, p.N, p.K,
+                                                                  group, nfull, total, ep);
   return cudaGetLastError();
+}
+
+template <int OP>
+static cudaError_t launch_16(const GemmPlan& p, cudaStream_t s) {
+  if (p.bn == 256) {
+    switch (p.epi) {
+      case EPI_F16: return launch_t<256, EPI_F16, OP>(p, s);
+      case EPI_F32: return launch_t<256, EPI_F32, OP>(p, s);
+      case EPI_RESID: return launch_t<256, EPI_RESID, OP>(p, s);
+      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, OP>(p, s);
+      case EPI_QKV: return launch_t<256, EPI_QKV, OP>(p, s);
+    }
+  } else {
+    switch (p.epi) {
+      case EPI_F16: return launch_t<128, EPI_F16, OP>(p, s);
+      case EPI_F32: return launch_t<128, EPI_F32, OP>(p, s);
+      case EPI_RESID: return launch_t<128, EPI_RESID, OP>(p, s);
+      case EPI_SWIGLU: return launch_t<128, EPI_SWIGLU, OP>(p, s);
+      case EPI_QKV: return launch_t<128, EPI_QKV, OP>(p, s);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
@@ -627,31 +711,14 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
   if (p.f8) {
     if (p.bn != 256) return cudaErrorInvalidValue;
     switch (p.epi) {
-      case EPI_F32: return launch_t<256, EPI_F32, true>(p, s);
-      case EPI_RESID: return launch_t<256, EPI_RESID, true>(p, s);
-      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, true>(p, s);
-      case EPI_QKV: return launch_t<256, EPI_QKV, true>(p, s);
+      case EPI_F32: return launch_t<256, EPI_F32, kOpF8>(p, s);
+      case EPI_RESID: return launch_t<256, EPI_RESID, kOpF8>(p, s);
+      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, kOpF8>(p, s);
+      case EPI_QKV: return launch_t<256, EPI_QKV, kOpF8>(p, s);
     }
     return cudaErrorInvalidValue;
   }
-  if (p.bn == 256) {
-    switch (p.epi) {
-      case EPI_F16: return launch_t<256, EPI_F16>(p, s);
-      case EPI_F32: return launch_t<256, EPI_F32>(p, s);
-      case EPI_RESID: return launch_t<256, EPI_RESID>(p, s);
-      case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU>(p, s);
-      case EPI_QKV: return launch_t<256, EPI_QKV>(p, s);
-    }
-  } else {
-    switch (p.epi) {
-      case EPI_F16: return launch_t<128, EPI_F16>(p, s);
-      case EPI_F32: return launch_t<128, EPI_F32>(p, s);
-      case EPI_RESID: return launch_t<128, EPI_RESID>(p, s);
-      case EPI_SWIGLU: return launch_t<128, EPI_SWIGLU>(p, s);
-      case EPI_QKV: return launch_t<128, EPI_QKV>(p, s);
-    }
-  }
-  return cudaErrorInvalidValue;
+  return p.dt == DT_BF16 ? launch_16<kOpBF16>(p, s) : launch_16<kOpF16>(p, s);
 }
 
 }  // namespace qi21

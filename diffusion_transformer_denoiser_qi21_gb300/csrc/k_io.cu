@@ -250,22 +250,25 @@ cudaError_t launch_timestep(int dim, float t, const float* t_lin1, const float* 
 
 // ------------------------------------------------------- finite check ----
 // Counts NaN/Inf values by their exponent bits (all ones), so no floating
-// point is involved: f32 0x7f800000, f16 0x7c00. 16-byte loads over the
-// aligned body, scalar loads over the unaligned head and the tail; one
-// atomic per warp into a file-scope counter.
+// point is involved: f32 0x7f800000, f16 0x7c00, bf16 0x7f80. 16-byte loads
+// over the aligned body, scalar loads over the unaligned head and the tail;
+// one atomic per warp into a file-scope counter. KIND: 4 f32, 2 f16,
+// 3 bf16.
 static __device__ unsigned long long g_nonfinite;
 
 __global__ void zero_count_kernel() { g_nonfinite = 0ull; }
 
-template <int EB>
+template <int KIND>
 __device__ __forceinline__ unsigned bad_elem(const uint8_t* p) {
-  if (EB == 4) return (*reinterpret_cast<const uint32_t*>(p) & 0x7f800000u) == 0x7f800000u;
-  return (*reinterpret_cast<const uint16_t*>(p) & 0x7c00u) == 0x7c00u;
+  if (KIND == 4) return (*reinterpret_cast<const uint32_t*>(p) & 0x7f800000u) == 0x7f800000u;
+  constexpr uint16_t m = KIND == 3 ? 0x7f80u : 0x7c00u;
+  return (*reinterpret_cast<const uint16_t*>(p) & m) == m;
 }
 
-template <int EB>
+template <int KIND>
 __global__ void __launch_bounds__(256) count_nonfinite_kernel(const uint8_t* __restrict__ x, size_t count,
                                                               size_t head, size_t nvec) {
+  constexpr int EB = KIND == 4 ? 4 : 2;
   constexpr int kPer = 16 / EB;
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nth = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(256) count_nonfinite_kernel(const uint8_t* __r
   const size_t tail0 = head + nvec * kPer;
   for (size_t i = tid; i < head + (count - tail0); i += nth) {
     const size_t e = i < head ? i : tail0 + (i - head);
-    bad += bad_elem<EB>(x + e * EB);
+    bad += bad_elem<KIND>(x + e * EB);
   }
   const uint4* v = reinterpret_cast<const uint4*>(x + head * EB);
   for (size_t i = tid; i < nvec; i += nth) {
@@ -282,11 +285,12 @@ __global__ void __launch_bounds__(256) count_nonfinite_kernel(const uint8_t* __r
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      if (EB == 4) {
+      if (KIND == 4) {
         bad += (w[k] & 0x7f800000u) == 0x7f800000u;
       } else {
-        bad += (w[k] & 0x7c00u) == 0x7c00u;
-        bad += (w[k] & 0x7c000000u) == 0x7c000000u;
+        constexpr uint32_t m = KIND == 3 ? 0x7f80u : 0x7c00u;
+        bad += (w[k] & m) == m;
+        bad += (w[k] & (m << 16)) == (m << 16);
       }
     }
   }
@@ -295,20 +299,24 @@ __global__ void __launch_bounds__(256) count_nonfinite_kernel(const uint8_t* __r
   if ((threadIdx.x & 31) == 0 && bad) atomicAdd(&g_nonfinite, static_cast<unsigned long long>(bad));
 }
 
-cudaError_t count_nonfinite(const void* x, size_t count, int elem_bytes, unsigned long long* out,
-                            cudaStream_t s) {
+cudaError_t count_nonfinite(const void* x, size_t count, int elem, unsigned long long* out, cudaStream_t s) {
+  if (elem != 2 && elem != 3 && elem != 4) return cudaErrorInvalidValue;
+  const int elem_bytes = elem == 4 ? 4 : 2;
   const uintptr_t a = reinterpret_cast<uintptr_t>(x);
   size_t head = ((16 - (a & 15)) & 15) / elem_bytes;
   if (head > count) head = count;
   const size_t nvec = (count - head) / (16 / elem_bytes);
   const size_t work = nvec + head + 1;
-  const unsigned grid = static_cast<unsigned>(std::min<size_t>((work + 255) / 256, 152 * 8));
+  const unsigned grid = static_cast<unsigned>(std::min<size_t>((work + 255) / 256, static_cast<size_t>(sm_count()) * 8));
   zero_count_kernel<<<1, 1, 0, s>>>();
   if (count > 0) {
-    if (elem_bytes == 4)
-      count_nonfinite_kernel<4><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(x), count, head, nvec);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    if (elem == 4)
+      count_nonfinite_kernel<4><<<grid, 256, 0, s>>>(xb, count, head, nvec);
+    else if (elem == 3)
+      count_nonfinite_kernel<3><<<grid, 256, 0, s>>>(xb, count, head, nvec);
     else
-      count_nonfinite_kernel<2><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(x), count, head, nvec);
+      count_nonfinite_kernel<2><<<grid, 256, 0, s>>>(xb, count, head, nvec);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -2,6 +2,7 @@
 // modulated LayerNorm, the per-head qk RMSNorm + interleaved RoPE, the K/V
 // cache copy and the gate/up plane interleave. All HBM-bound: 128-bit
 // coalesced loads/stores, one CTA per row where a row reduction is needed.
+// The 16-bit rows are f16 or bf16 (the geometry's dtype, template BF).
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -35,8 +36,9 @@ cudaError_t launch_mods_prep(int dim, const float* mods, float* md, cudaStream_t
 // held in registers (NV float4 per thread, NV = dim / 1024 rounded up to a
 // power of two, dim <= 8192):
 //   if y:  x += gate_t * y            (qwen_image21.rs, Qi21Dit::gated_add)
-//   if xn: xn = f16(LN(x) (1 + scale)) (Qi21Dit::norm_mod; affine-free LN,
-//          biased variance, two passes over the registers in f32)
+//   if xn: xn = LN(x) (1 + scale) rounded to f16 / bf16 (Qi21Dit::norm_mod;
+//          affine-free LN, biased variance, two passes over the registers
+//          in f32)
 constexpr int kRowThreads = 256;
 
 __device__ __forceinline__ float block_sum_256(float v, float* red) {
@@ -52,12 +54,10 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 // resident CTAs per SM: four, two for the widest rows (register budget)
 constexpr int rowop_ctas_per_sm(int nv) { return nv >= 8 ? 2 : 4; }
 
-template <int NV>
-__global__ void __launch_bounds__(kRowThreads, rowop_ctas_per_sm(NV)) rowop_kernel(int rows, int dim, float eps, float* __restrict__ x,
-                                                               const float* __restrict__ y,
-                                                               const float* __restrict__ gate_t,
-                                                               const float* __restrict__ scale,
-                                                               __half* __restrict__ xn) {
+template <int NV, bool BF>
+__global__ void __launch_bounds__(kRowThreads, rowop_ctas_per_sm(NV))
+    rowop_kernel(int rows, int dim, float eps, float* __restrict__ x, const float* __restrict__ y,
+                 const float* __restrict__ gate_t, const float* __restrict__ scale, uint16_t* __restrict__ xn) {
   __shared__ float red[8];
   const int nv = dim >> 2;
   // rows blockIdx.x, + gridDim.x, ...: the next row's x is loaded while
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kRowThreads, rowop_ctas_per_sm(NV)) rowop_kern
         if (idx < nv) {
           const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
           uint2 out;
-          out.x = pack_half2((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
-          out.y = pack_half2((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
+          out.x = pack2<BF>((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
+          out.y = pack2<BF>((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
           o2[idx] = out;
         }
       }
@@ -251,29 +251,41 @@ cudaError_t launch_quant_rows(int rows, int cols, const __half* a, size_t lda, u
   return cudaGetLastError();
 }
 
-cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
-                         const float* scale, __half* xn, cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
+template <bool BF>
+static void rowop_go(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
+                     const float* scale, uint16_t* xn, cudaStream_t s) {
   const int per = (dim / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
   // all CTAs resident, each walking rows with a stride of the grid
   auto grid = [&](int nv) { return std::min(rows, rowop_ctas_per_sm(nv) * sm_count()); };
   if (per <= 1)
-    rowop_kernel<1><<<grid(1), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<1, BF><<<grid(1), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else if (per <= 2)
-    rowop_kernel<2><<<grid(2), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<2, BF><<<grid(2), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else if (per <= 4)
-    rowop_kernel<4><<<grid(4), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<4, BF><<<grid(4), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
   else
-    rowop_kernel<8><<<grid(8), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
+    rowop_kernel<8, BF><<<grid(8), kRowThreads, 0, s>>>(rows, dim, eps, x, y, gate_t, scale, xn);
+}
+
+cudaError_t launch_rowop(int rows, int dim, float eps, float* x, const float* y, const float* gate_t,
+                         const float* scale, void* xn, int dt, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (dt != DT_F16 && dt != DT_BF16) return cudaErrorInvalidValue;
+  uint16_t* o = static_cast<uint16_t*>(xn);
+  if (dt == DT_BF16)
+    rowop_go<true>(rows, dim, eps, x, y, gate_t, scale, o, s);
+  else
+    rowop_go<false>(rows, dim, eps, x, y, gate_t, scale, o, s);
   return cudaGetLastError();
 }
 
 // --------------------------------------------------------------- qkrope ----
 // One 256-thread CTA per panel row; each warp takes head vectors of q then
-// k (128 f16 = 4 per lane), RMSNorm over the 128 values (warp shuffle), the
-// weight, then rotates the pairs (2j, 2j+1) by the row's angle j
+// k (128 values = 4 per lane), RMSNorm over the 128 values (warp shuffle),
+// the weight, then rotates the pairs (2j, 2j+1) by the row's angle j
 // (qwen_image21.rs, Qi21Dit::qk_norm_rope; gpu_wgpu/qi21.rs, zi_qkrope).
-__global__ void __launch_bounds__(256) qkrope_kernel(int heads, float eps, __half* __restrict__ panel,
+template <bool BF>
+__global__ void __launch_bounds__(256) qkrope_kernel(int heads, float eps, uint16_t* __restrict__ panel,
                                                      const float* __restrict__ norm_q,
                                                      const float* __restrict__ norm_k,
                                                      RopeTables tabs) {
@@ -290,12 +302,12 @@ __global__ void __launch_bounds__(256) qkrope_kernel(int heads, float eps, __hal
   const float4 wq = reinterpret_cast<const float4*>(norm_q)[lane];
   const float4 wk = reinterpret_cast<const float4*>(norm_k)[lane];
   const int H = heads * 128;
-  __half* base = panel + static_cast<size_t>(row) * 3 * H;
+  uint16_t* base = panel + static_cast<size_t>(row) * 3 * H;
   for (int v = warp; v < 2 * heads; v += 8) {
     uint2* p = reinterpret_cast<uint2*>(base + v * 128 + lane * 4);
     const uint2 raw = *p;
-    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    const float2 lo = unpack2<BF>(raw.x);
+    const float2 hi = unpack2<BF>(raw.y);
     float ss = (lo.x * lo.x + lo.y * lo.y) + (hi.x * hi.x + hi.y * hi.y);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -304,24 +316,29 @@ __global__ void __launch_bounds__(256) qkrope_kernel(int heads, float eps, __hal
     const float a0 = lo.x * inv * w.x, a1 = lo.y * inv * w.y;
     const float a2 = hi.x * inv * w.z, a3 = hi.y * inv * w.w;
     uint2 out;
-    out.x = pack_half2(a0 * c.x - a1 * sn.x, a0 * sn.x + a1 * c.x);
-    out.y = pack_half2(a2 * c.y - a3 * sn.y, a2 * sn.y + a3 * c.y);
+    out.x = pack2<BF>(a0 * c.x - a1 * sn.x, a0 * sn.x + a1 * c.x);
+    out.y = pack2<BF>(a2 * c.y - a3 * sn.y, a2 * sn.y + a3 * c.y);
     *p = out;
   }
 }
 
-cudaError_t launch_qkrope(int rows, int heads, float eps, __half* panel, const float* norm_q,
+cudaError_t launch_qkrope(int rows, int heads, float eps, void* panel, int dt, const float* norm_q,
                           const float* norm_k, const RopeTables& tabs, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  qkrope_kernel<<<rows, 256, 0, s>>>(heads, eps, panel, norm_q, norm_k, tabs);
+  if (dt != DT_F16 && dt != DT_BF16) return cudaErrorInvalidValue;
+  uint16_t* pp = static_cast<uint16_t*>(panel);
+  if (dt == DT_BF16)
+    qkrope_kernel<true><<<rows, 256, 0, s>>>(heads, eps, pp, norm_q, norm_k, tabs);
+  else
+    qkrope_kernel<false><<<rows, 256, 0, s>>>(heads, eps, pp, norm_q, norm_k, tabs);
   return cudaGetLastError();
 }
 
 // --------------------------------------------------------------- kvcopy ----
 // The K|V columns of the panel -> the layer's cache row, 16 B per thread
-// (gpu_wgpu/qi21.rs, qi_kvcopy).
-__global__ void kvcopy_kernel(int rows, int dim, const __half* __restrict__ panel,
-                              __half* __restrict__ kv) {
+// (gpu_wgpu/qi21.rs, qi_kvcopy); 16-bit elements of either type.
+__global__ void kvcopy_kernel(int rows, int dim, const uint16_t* __restrict__ panel,
+                              uint16_t* __restrict__ kv) {
   const int per_row = (2 * dim) / 8;  // uint4 per cache row
   const size_t total = static_cast<size_t>(rows) * per_row;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
@@ -333,32 +350,32 @@ __global__ void kvcopy_kernel(int rows, int dim, const __half* __restrict__ pane
   }
 }
 
-cudaError_t launch_kvcopy(int rows, int dim, const __half* panel, __half* kv, cudaStream_t s) {
+cudaError_t launch_kvcopy(int rows, int dim, const void* panel, void* kv, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const size_t total = static_cast<size_t>(rows) * (2 * dim / 8);
-  const int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, 152 * 16));
-  kvcopy_kernel<<<grid, 256, 0, s>>>(rows, dim, panel, kv);
+  const int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(sm_count()) * 16));
+  kvcopy_kernel<<<grid, 256, 0, s>>>(rows, dim, static_cast<const uint16_t*>(panel), static_cast<uint16_t*>(kv));
   return cudaGetLastError();
 }
 
 // -------------------------------------------------------------- pack w13 ----
 // Interleave gate and up in 64-row blocks so that every 128-row slice of the
 // plane holds a matching (gate, up) pair for the SwiGLU epilogue.
-__global__ void pack_w13_kernel(int inter, int dim, const __half* __restrict__ gate,
-                                const __half* __restrict__ up, __half* __restrict__ dst) {
+__global__ void pack_w13_kernel(int inter, int dim, const uint16_t* __restrict__ gate,
+                                const uint16_t* __restrict__ up, uint16_t* __restrict__ dst) {
   const int r = blockIdx.x;  // destination row in [0, 2I)
   const int j = r >> 7;
   const int w = r & 127;
-  const __half* src = (w < 64) ? gate + static_cast<size_t>(64 * j + w) * dim
-                               : up + static_cast<size_t>(64 * j + (w - 64)) * dim;
+  const uint16_t* src = (w < 64) ? gate + static_cast<size_t>(64 * j + w) * dim
+                                 : up + static_cast<size_t>(64 * j + (w - 64)) * dim;
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * dim);
   for (int c = threadIdx.x; c < dim / 8; c += blockDim.x) d4[c] = s4[c];
 }
 
-cudaError_t launch_pack_w13(int inter, int dim, const __half* gate, const __half* up, __half* dst,
-                            cudaStream_t s) {
-  pack_w13_kernel<<<2 * inter, 256, 0, s>>>(inter, dim, gate, up, dst);
+cudaError_t launch_pack_w13(int inter, int dim, const void* gate, const void* up, void* dst, cudaStream_t s) {
+  pack_w13_kernel<<<2 * inter, 256, 0, s>>>(inter, dim, static_cast<const uint16_t*>(gate),
+                                            static_cast<const uint16_t*>(up), static_cast<uint16_t*>(dst));
   return cudaGetLastError();
 }
 

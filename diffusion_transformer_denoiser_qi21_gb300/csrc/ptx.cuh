@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -76,6 +77,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait for a phase without regard to the abort flag, for a role that gave
+// up and must still let copies it started finish before its CTA leaves:
+// bounded by kWaitTimeoutNs; false if the phase did not complete.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(a, parity))
+    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
@@ -90,18 +102,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// Same tile, multicast: the box lands at the same shared-memory offset in
-// every CTA of `mask` (bit i = cluster rank i), and each destination CTA's
-// mbarrier at `bar`'s offset receives the bytes it got.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                               int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
 }
 
@@ -205,16 +205,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "memory");
 }
 
-// As tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// `mask` (bit i = cluster rank i).
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // Pair forms (cta_group::2): TMEM allocation jointly by one warp of each CTA
 // of the pair, MMAs issued by one thread of the even CTA over both CTAs'
 // shared memory and TMEM, commits arriving on both CTAs' barriers.
@@ -288,12 +278,12 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// Instruction descriptor of kind::f16: f16 A and B, f32 D, both operands
-// K-major unless b_mn_major, shape M x N (x16).
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false) {
-  return (1u << 4)                       // D format: f32
-         | (0u << 7) | (0u << 10)        // A, B format: f16
-         | (0u << 15)                    // A K-major
+// Instruction descriptor of kind::f16: f16 (or, with bf16, bf16) A and B,
+// f32 D, both operands K-major unless b_mn_major, shape M x N (x16).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false, bool bf16 = false) {
+  return (1u << 4)                                                  // D format: f32
+         | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10)     // A, B format: f16 0, bf16 1
+         | (0u << 15)                                               // A K-major
          | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -381,6 +371,30 @@ __device__ __forceinline__ int e4m3_row_exp(float amax) {
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two values rounded (to nearest even) to the 16-bit type of the pass
+// (bf16 if BF, else f16), value a in the low half.
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF)
+    return pack_bf162(a, b);
+  else
+    return pack_half2(a, b);
+}
+
+// The two 16-bit values of a packed pair widened to f32 (low half first).
+template <bool BF>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF)
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  else
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 }  // namespace qi21

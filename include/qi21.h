@@ -23,14 +23,22 @@
  *    mask, too-small workspace) nothing is written and nothing is enqueued;
  *    the function returns a negative QI21_ERR_* and qi21_last_error()
  *    (thread-local) describes it. This mirrors the page's "decline, no
- *    partial results" convention.
+ *    partial results" convention. A pass (prefill, step, denoiser call)
+ *    validates every layer and encodes every layer's tensor maps before it
+ *    enqueues its first copy or kernel, so a failure found at any layer
+ *    leaves the stream untouched.
  *  - Every spin-wait inside the kernels gives up after about 2 s and raises
  *    a device status word; qi21_device_status() reads and clears it.
  *  - Entry points may be called from several host threads at once, each on
  *    its own stream and buffers; the library's one-time set-up is
- *    thread-safe. A thread with no current CUDA context gets the current
- *    device's primary context bound on its first call (as the CUDA runtime
- *    does on a thread's first runtime call).
+ *    thread-safe and kept per device (kernel attributes, SM count), so one
+ *    process may drive several devices, each call working on the current
+ *    one. A thread with no current CUDA context gets the current device's
+ *    primary context bound on its first call (as the CUDA runtime does on a
+ *    thread's first runtime call).
+ *  - Every layer of a pass is bracketed by an NVTX range ("qi21 prefill
+ *    layer l" / "qi21 step layer l"), visible to a profiler that collects
+ *    NVTX and free otherwise.
  */
 #ifndef QI21_H
 #define QI21_H
@@ -58,11 +66,21 @@ extern "C" {
 #define QI21_SEG_TEXT 0  /* a = number of text rows, b unused */
 #define QI21_SEG_IMAGE 1 /* a = h, b = w; h*w rows in raster order */
 
+/* 16-bit element types (qi21_geom::dtype). */
+#define QI21_DTYPE_F16 0  /* IEEE half */
+#define QI21_DTYPE_BF16 1 /* bfloat16 (8-bit exponent, 7-bit mantissa) */
+
 /* Model geometry (qwen_image21.rs, Qi21Config). Kernel limits (the page's
  * geom_ok, gpu_wgpu/qi21.rs): head_dim == 128, heads*head_dim == dim,
  * dim % 128 == 0, 128 <= dim <= 8192, mlp_hidden % 64 == 0, axes even and
- * summing to head_dim, layers >= 1. Compute type: f16 operands, f32
- * accumulation, f32 residual stream. */
+ * summing to head_dim, layers >= 1, dtype QI21_DTYPE_F16 or _BF16.
+ * Compute type: 16-bit operands of `dtype` (weight planes, the modulated-LN
+ * rows, the qkv panel, the attention output, the SwiGLU hidden rows and
+ * the K/V cache), f32 accumulation, f32 residual stream. The page's device
+ * path converts F16 / Bf16 / F32 container weights into f16 planes
+ * (gpu_wgpu/qi21.rs module notes, ZBlockDev::from_model_all); the bf16
+ * type here keeps bf16 weights as they are, with bf16's f32-wide exponent
+ * range in place of f16's range. */
 typedef struct qi21_geom {
   int32_t dim;        /* H */
   int32_t heads;      /* nh */
@@ -72,6 +90,7 @@ typedef struct qi21_geom {
   int32_t axes[3];    /* RoPE axis widths (frame, h, w), e.g. 16, 56, 56 */
   float eps;          /* LayerNorm / RMSNorm epsilon, e.g. 1e-6 */
   float theta;        /* RoPE base, e.g. 10000 */
+  int32_t dtype;      /* QI21_DTYPE_F16 (0) or QI21_DTYPE_BF16 (1) */
 } qi21_geom;
 
 /* One run of the joint sequence (qwen_image21.rs, enum Seg). The last
@@ -82,13 +101,14 @@ typedef struct qi21_seg {
   int32_t b;
 } qi21_seg;
 
-/* Device planes of one block, as produced by qi21_pack_layer.
- *   wqkv  f16 [3H][H]  rows q (H), k (H), v (H)
- *   wo    f16 [H][H]
- *   w13   f16 [2I][H]  gate/up interleaved in 64-row blocks:
- *                      rows [128j, 128j+64) = gate rows [64j, 64j+64),
- *                      rows [128j+64, 128j+128) = up rows [64j, 64j+64)
- *   w2    f16 [H][I]   (down)
+/* Device planes of one block, as produced by qi21_pack_layer, in the
+ * geometry's 16-bit dtype (T below):
+ *   wqkv  T [3H][H]  rows q (H), k (H), v (H)
+ *   wo    T [H][H]
+ *   w13   T [2I][H]  gate/up interleaved in 64-row blocks:
+ *                    rows [128j, 128j+64) = gate rows [64j, 64j+64),
+ *                    rows [128j+64, 128j+128) = up rows [64j, 64j+64)
+ *   w2    T [H][I]   (down)
  *   norm_q, norm_k  f32 [128] per-head RMSNorm weights (used as is)
  * Tensor names on the page: attn.to_q/to_k/to_v, attn.to_out.0,
  * img_mlp.gate_layer (gate), img_mlp.proj (up), img_mlp.out (down),
@@ -102,7 +122,8 @@ typedef struct qi21_layer {
   const float* norm_k;
 } qi21_layer;
 
-/* Opaque per-prompt cache: L layers of post-RoPE K|V, f16 [lp][2H] each
+/* Opaque per-prompt cache: L layers of post-RoPE K|V, [lp][2H] each in the
+ * geometry's dtype
  * (K in columns [0, H), V in [H, 2H)), plus the layout, the prefix
  * visibility and the RoPE tables of the prefix rows and of the target rows
  * at the positions after THIS prefix (qwen_image21.rs, struct Qi21Prefix). */
@@ -139,7 +160,7 @@ int qi21_layout_indices(const qi21_seg* segs, int32_t nseg, const int32_t axes[3
                         int64_t* pos, int32_t* block_ids, uint32_t* vis, float* cos_,
                         float* sin_);
 
-/* Bytes of one layer's packed planes (wqkv + wo + w13 + w2, f16, each
+/* Bytes of one layer's packed planes (wqkv + wo + w13 + w2, 16-bit, each
  * 256-byte aligned). */
 size_t qi21_layer_plane_bytes(const qi21_geom* g);
 
@@ -149,7 +170,8 @@ size_t qi21_workspace_bytes(const qi21_geom* g, int32_t max_rows);
 
 /* ----------------------------------------------------------- device ---- */
 
-/* Pack one layer's weights (device f16, nn.Linear layout: wq/wk/wv/wo
+/* Pack one layer's weights (device, the geometry's dtype, nn.Linear
+ * layout: wq/wk/wv/wo
  * [H][H], wgate/wup [I][H], wdown [H][I]; norm_q/norm_k device f32 [128])
  * into `planes` (device, >= qi21_layer_plane_bytes, 256-byte aligned) and
  * fill `out` with pointers into it (norm_q/norm_k are referenced, not
@@ -173,8 +195,8 @@ void qi21_kvcache_free(qi21_kvcache* c);
 /* Prefix rows, target rows and layers of a cache; any pointer may be NULL. */
 int qi21_kvcache_info(const qi21_kvcache* c, int32_t* lp, int32_t* n, int32_t* layers);
 
-/* Device pointer of layer `layer`'s K|V block, f16 [lp][2H] (read-only use
- * by the caller: parity checks, saving a prompt). */
+/* Device pointer of layer `layer`'s K|V block, [lp][2H] of the geometry's
+ * dtype (read-only use by the caller: parity checks, saving a prompt). */
 int qi21_kvcache_layer(const qi21_kvcache* c, int32_t layer, const void** kv);
 
 /* Prefill (qwen_image21.rs, Qi21Dit::prefill; gpu_wgpu/qi21.rs, prefill and
@@ -314,11 +336,16 @@ int qi21_timestep_mods(int32_t dim, float t, const float* t_lin1, const float* t
 #define QI21_CHECK_FINITE 1u
 uint32_t qi21_set_checks(uint32_t flags);
 
-/* Number of NaN/infinite values among `count` device elements of x (f32
- * when elem_bytes == 4, f16 when 2; x aligned to its element). Enqueues the
- * scan on stream, synchronises the stream and writes the count to
- * *out_count (host). Calls from several host threads are serialised. */
-int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_bytes, uint64_t* out_count,
+/* Element types of qi21_count_nonfinite. */
+#define QI21_ELEM_F16 2
+#define QI21_ELEM_BF16 3
+#define QI21_ELEM_F32 4
+
+/* Number of NaN/infinite values among `count` device elements of x of type
+ * elem_type (QI21_ELEM_F32, _F16 or _BF16; x aligned to its element).
+ * Enqueues the scan on stream, synchronises the stream and writes the count
+ * to *out_count (host). Calls from several host threads are serialised. */
+int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_type, uint64_t* out_count,
                          void* stream);
 
 /* A recorded call (this library's addition: the page replays command
@@ -359,7 +386,8 @@ void qi21_graph_free(qi21_graph* graph);
  * accumulation) and the epilogue applies both scales. The attention, the
  * norms, the residual stream and the K/V cache are as in the f16 path. Not
  * the headline precision: its per-block error is set by the 3-bit mantissa
- * (about 2^-5 relative per operand element), not by the f16 bar. */
+ * (about 2^-5 relative per operand element), not by the f16 bar. The FP8
+ * entry points take f16 geometries only (QI21_ERR_GEOM for bf16). */
 
 /* E4M3 planes of one layer: codes with the shapes of qi21_layer's planes
  * (wqkv [3H][H], wo [H][H], w13 [2I][H] interleaved, w2 [H][I]) and one f32
@@ -452,14 +480,15 @@ int qi21_profile_read(float* ms, int64_t* launches);
 
 /* ------------------------------------------------- single operations ---- */
 /* Kernel-level entry points (the same kernels the passes launch), for
- * per-operation parity checks and profiling. All pointers are device. */
+ * per-operation parity checks and profiling. All pointers are device;
+ * `dtype` (QI21_DTYPE_*) is the type of the 16-bit operands (T). */
 
-/* xn = f16(LN(x)(1 + scale)) per row; if y != NULL it first does
+/* xn = T(LN(x)(1 + scale)) per row; if y != NULL it first does
  * x += gate_t * y in place (gate_t = tanh of the raw gate, f32 [H]).
- * x f32 [rows][H], y f32 [rows][H], scale f32 [H], xn f16 [rows][H] (may be
+ * x f32 [rows][H], y f32 [rows][H], scale f32 [H], xn T [rows][H] (may be
  * NULL when y != NULL). qwen_image21.rs: Qi21Dit::norm_mod, gated_add;
  * gpu_wgpu/qi21.rs: qi_rowop. */
-int qi21_op_rowop(int32_t rows, int32_t dim, float eps, float* x, const float* y,
+int qi21_op_rowop(int32_t dtype, int32_t rows, int32_t dim, float eps, float* x, const float* y,
                   const float* gate_t, const float* scale, void* xn, void* stream);
 
 /* md = [s1 | tanh g1 | s2 | tanh g2] from raw mods, f32 [4H] each
@@ -467,24 +496,25 @@ int qi21_op_rowop(int32_t rows, int32_t dim, float eps, float* x, const float* y
 int qi21_op_mods_prep(int32_t dim, const float* mods, float* md, void* stream);
 
 /* GEMM epilogues of qi21_op_gemm. */
-#define QI21_EPI_F16 0    /* out f16 [M][ldo] = acc */
+#define QI21_EPI_F16 0    /* out T [M][ldo] = acc (T = the operands' type) */
 #define QI21_EPI_F32 1    /* out f32 [M][ldo] = acc */
 #define QI21_EPI_RESID 2  /* out f32 [M][ldo] += gate_t[col] * acc */
-#define QI21_EPI_SWIGLU 3 /* out f16 [M][ldo]: col 64j+c = silu(acc[128j+c]) *
+#define QI21_EPI_SWIGLU 3 /* out T [M][ldo]: col 64j+c = silu(acc[128j+c]) *
                              acc[128j+64+c] (N = 2*I on the interleaved plane) */
 
-/* acc = A B^T with A f16 [M][K] (row stride K), B f16 [N][K] (row stride
- * K), f32 accumulation on the tensor cores; M >= 1, N % 128 == 0,
+/* acc = A B^T with A T [M][K] (row stride K), B T [N][K] (row stride K),
+ * f32 accumulation on the tensor cores; M >= 1, N % 128 == 0,
  * K % 64 == 0. */
-int qi21_op_gemm(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B,
-                 void* out, int32_t ldo, const float* gate_t, void* stream);
+int qi21_op_gemm(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, const void* A,
+                 const void* B, void* out, int32_t ldo, const float* gate_t, void* stream);
 
-/* In place on the panel f16 [rows][3H] (q in columns [0, H), k in [H, 2H)):
+/* In place on the panel T [rows][3H] (q in columns [0, H), k in [H, 2H)):
  * per (row, head) RMSNorm * norm_q (or norm_k) over 128 values, then the
  * interleaved RoPE of pairs (2j, 2j+1) by the row's cos/sin [rows][64]
  * (qwen_image21.rs, Qi21Dit::qk_norm_rope; gpu_wgpu/qi21.rs, zi_qkrope). */
-int qi21_op_qkrope(int32_t rows, int32_t heads, float eps, void* panel, const float* norm_q,
-                   const float* norm_k, const float* cos_, const float* sin_, void* stream);
+int qi21_op_qkrope(int32_t dtype, int32_t rows, int32_t heads, float eps, void* panel,
+                   const float* norm_q, const float* norm_k, const float* cos_, const float* sin_,
+                   void* stream);
 
 /* FP8 variant, single operations. qi21_op_quant_rows: f16 a [rows][cols]
  * (cols % 8 == 0) -> E4M3 codes q [rows][cols] and qs[row] = 2^e.
@@ -499,20 +529,20 @@ int qi21_op_gemm_fp8(int32_t epi, int32_t M, int32_t N, int32_t K, const void* A
                      const void* B, const float* sw, void* out, int32_t ldo, const float* gate,
                      void* stream);
 
-/* cache f16 [rows][2H] = panel columns [H, 3H) (gpu_wgpu/qi21.rs,
- * qi_kvcopy). */
+/* cache [rows][2H] = panel columns [H, 3H), 16-bit elements of either
+ * type (gpu_wgpu/qi21.rs, qi_kvcopy). */
 int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void* stream);
 
 /* Attention of nq query rows of the panel (q at columns [0, H) of panel
- * f16 [.][3H]) over n_pre keys from kv_pre (f16 [n_pre][2H], K then V; may
- * be NULL when n_pre == 0) followed by the panel's own keys rows
- * [0, n_own) (K at columns [H, 2H), V at [2H, 3H)). Query i sees keys
- * [0, vis[i]) if vis != NULL (uint32 [nq], non-decreasing, >= 1), else all
- * n_pre + n_own keys. out f16 [nq][H] (qwen_image21.rs, Qi21Dit::attention;
+ * T [.][3H]) over n_pre keys from kv_pre (T [n_pre][2H], K then V; may be
+ * NULL when n_pre == 0) followed by the panel's own keys rows [0, n_own)
+ * (K at columns [H, 2H), V at [2H, 3H)). Query i sees keys [0, vis[i]) if
+ * vis != NULL (uint32 [nq], non-decreasing, >= 1), else all n_pre + n_own
+ * keys. out T [nq][H] (qwen_image21.rs, Qi21Dit::attention;
  * gpu_wgpu/qi21.rs, qi_flash). */
-int qi21_op_attention(int32_t nq, int32_t heads, const void* panel, const void* kv_pre,
-                      int32_t n_pre, int32_t n_own, const uint32_t* vis, void* out,
-                      void* stream);
+int qi21_op_attention(int32_t dtype, int32_t nq, int32_t heads, const void* panel,
+                      const void* kv_pre, int32_t n_pre, int32_t n_own, const uint32_t* vis,
+                      void* out, void* stream);
 
 #ifdef __cplusplus
 }

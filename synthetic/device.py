@@ -11,12 +11,12 @@ from . import qi21_inputs as S
 
 def geom_of(w: S.Workload):
     import diffusion_transformer_denoiser_qi21_gb300 as q
-    return q.geom(w.dim, w.heads, w.mlp_hidden, w.layers, w.axes, w.eps, w.theta, w.head_dim)
+    return q.geom(w.dim, w.heads, w.mlp_hidden, w.layers, w.axes, w.eps, w.theta, w.head_dim, dtype=w.dtype)
 
 
-def _pinned_f16(shape):
+def _pinned_16(shape, dtype):
     import torch
-    return torch.empty(shape, dtype=torch.float16, pin_memory=True)
+    return torch.empty(shape, dtype=torch.float16 if dtype == "f16" else torch.int16, pin_memory=True)
 
 
 def upload_layer(w: S.Workload, layer: int, g, stream=None):
@@ -27,9 +27,11 @@ def upload_layer(w: S.Workload, layer: int, g, stream=None):
     dev = {}
     for tag in S.WEIGHT_TAGS:
         shape = S.weight_shape(w, tag)
-        host = _pinned_f16(shape)
-        S.weight(w, layer, tag, out=host.numpy())
-        dev[tag] = host.to("cuda", non_blocking=True)
+        host = _pinned_16(shape, w.dtype)
+        hv = host.numpy()
+        S.weight(w, layer, tag, out=hv if w.dtype == "f16" else hv.view(np.uint16))
+        d = host.to("cuda", non_blocking=True)
+        dev[tag] = d if w.dtype == "f16" else d.view(torch.bfloat16)
     nq = torch.from_numpy(S.norm_weight(w, layer, "norm_q")).cuda()
     nk = torch.from_numpy(S.norm_weight(w, layer, "norm_k")).cuda()
     packed = q.pack_layer(g, dev["wq"], dev["wk"], dev["wv"], dev["wo"], dev["wgate"], dev["wup"],

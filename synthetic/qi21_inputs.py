@@ -16,7 +16,8 @@ Recipe (one stream per tensor, so any single tensor can be rebuilt alone):
   float32, one set for the step (``mods_t``) and one for the t = 0 prefix
   (``mods0``);
 * projection weights ~ N(0, fan_in^-1/2) (standard deviation), rounded to
-  float16 (round to nearest even) -- the oracle widens exactly these values;
+  the workload's 16-bit type, float16 or bfloat16 (round to nearest even
+  from the float32 draw) -- the oracle widens exactly these values;
   fan_in = dim for q, k, v, o, gate, up and mlp_hidden for down;
 * per-head RMSNorm weights ``norm_q``, ``norm_k`` = 1 + N(0, 0.05) float32;
 * latent tokens ~ N(0, 1) float32 [n, 64]; img_in weight ~ N(0, 64^-1/2)
@@ -58,6 +59,7 @@ TAG_ID = {
     "modulation": 36,   # modulation.1
     "norm_out": 37,     # norm_out.linear
     "op_test": 50,  # single-operation checks: index = a case number
+    "sketch": 60,   # Gaussian sketch matrices of the parity statistics
 }
 
 # Segment kinds, as the library's C ABI numbers them.
@@ -82,6 +84,7 @@ class Workload:
     eps: float = 1e-6
     theta: float = 10000.0
     seed: int = 0
+    dtype: str = "f16"  # 16-bit type of the weights and activation rows: "f16" or "bf16"
 
     @property
     def nseq(self) -> int:
@@ -136,6 +139,25 @@ WORKLOADS = {
     "cfg_pair_d256": Workload("cfg_pair_d256", 256, 2, 768, 2, ((_t(18),), (_t(1),)), (9, 15)),
     # smallest target: one row, one-row prefix
     "single_row_d256": Workload("single_row_d256", 256, 2, 768, 1, ((_t(1),),), (1, 1)),
+    # one full-width block with the 4114-row condition prefix: every launch
+    # has the shapes of one layer of step32_cond4114_n4096 (small profiling
+    # captures of those kernels)
+    "block_cond4114_n4096": Workload(
+        "block_cond4114_n4096", 4096, 32, 12288, 1, ((_t(18), _i(64, 64)),), (64, 64)
+    ),
+    # --- bf16 weights and activation rows ---
+    "tiny_block_d256_bf16": Workload("tiny_block_d256_bf16", 256, 2, 768, 1, ((_t(18),),), (16, 16),
+                                     dtype="bf16"),
+    "chain32_d256_mixed_bf16": Workload(
+        "chain32_d256_mixed_bf16", 256, 2, 768, 32, ((_t(5), _i(4, 6), _t(3), _i(3, 2)),), (10, 13), dtype="bf16"
+    ),
+    "cfg_pair_d256_bf16": Workload("cfg_pair_d256_bf16", 256, 2, 768, 2, ((_t(18),), (_t(1),)), (9, 15),
+                                   dtype="bf16"),
+    "block_d4096_n4096_bf16": Workload("block_d4096_n4096_bf16", 4096, 32, 12288, 1, ((_t(18),),), (64, 64),
+                                       dtype="bf16"),
+    "step32_cond4114_n4096_bf16": Workload(
+        "step32_cond4114_n4096_bf16", 4096, 32, 12288, 32, ((_t(18), _i(64, 64)),), (64, 64), dtype="bf16"
+    ),
 }
 
 
@@ -248,12 +270,40 @@ def weight_shape(w: Workload, tag: str) -> tuple:
     }[tag]
 
 
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 values -> bfloat16 bit patterns (uint16), rounded to nearest
+    even (the draws hold no NaN)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> the same values as float32."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
 def weight(w: Workload, layer: int, tag: str, out: np.ndarray | None = None) -> np.ndarray:
-    """Projection weight of ``layer`` in nn.Linear layout [out, in], float16."""
+    """Projection weight of ``layer`` in nn.Linear layout [out, in], as the
+    device stores it: float16 for f16 workloads, bfloat16 bit patterns
+    (uint16) for bf16 workloads (into ``out`` if given)."""
     rows, cols = weight_shape(w, tag)
     flat = None if out is None else out.reshape(-1)
+    if w.dtype == "bf16":
+        z = normal(w.seed, tag, layer, rows * cols, cols ** -0.5)
+        b = bf16_bits(z)
+        if flat is not None:
+            flat[:] = b
+            b = flat
+        return b.reshape(rows, cols)
     res = normal(w.seed, tag, layer, rows * cols, cols ** -0.5, out=flat, dtype=np.float16)
     return res.reshape(rows, cols)
+
+
+def weight_values(w: Workload, layer: int, tag: str) -> np.ndarray:
+    """The values of ``weight``: float16, or float32 holding the bfloat16
+    values exactly."""
+    a = weight(w, layer, tag)
+    return bf16_values(a) if w.dtype == "bf16" else a
 
 
 def norm_weight(w: Workload, layer: int, tag: str) -> np.ndarray:
@@ -262,8 +312,9 @@ def norm_weight(w: Workload, layer: int, tag: str) -> np.ndarray:
 
 
 def layer_weights(w: Workload, layer: int) -> dict:
-    """All weights of one layer (float16 projections, float32 norms)."""
-    d = {t: weight(w, layer, t) for t in WEIGHT_TAGS}
+    """All weights of one layer (projection values as stored on the device:
+    float16, or bfloat16 values as float32; float32 norms)."""
+    d = {t: weight_values(w, layer, t) for t in WEIGHT_TAGS}
     d["norm_q"] = norm_weight(w, layer, "norm_q")
     d["norm_k"] = norm_weight(w, layer, "norm_k")
     return d
@@ -275,3 +326,12 @@ def op_tensor(seed: int, case: int, slot: int, shape, std: float = 1.0, offset: 
     slot) of the "op_test" tag."""
     count = int(np.prod(shape))
     return normal(seed * 1000003 + case, "op_test", slot, count, std, dtype=dtype, offset=offset).reshape(shape)
+
+
+def sketch(rows: int, k: int, side: int) -> np.ndarray:
+    """A seeded Gaussian sketch matrix float64 [k, rows] (N(0, 1) entries),
+    used by the parity tests to reduce a [rows, cols] output X to the small
+    matrix L X R^T (L = sketch(rows, k, 0), R = sketch(cols, k, 1)) whose
+    relative L2 difference estimates that of the whole output. Random
+    numbers only: stream (0, "sketch", rows * 4 + side) of the recipe."""
+    return normal(0, "sketch", rows * 4 + side, k * rows, 1.0).astype(np.float64).reshape(k, rows)

@@ -19,6 +19,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import diffusion_transformer_denoiser_qi21_gb300 as q  # noqa: E402
+from blockcheck import DeviceRun, end_to_end, host, sample_rows, teacher_forced_layer  # noqa: E402
 from oracle import qi21_oracle as O  # noqa: E402
 from synthetic import device as D  # noqa: E402
 from synthetic import qi21_inputs as S  # noqa: E402
@@ -30,97 +31,11 @@ DELTA_TOL = 1e-2
 KV_TOL = 2e-3
 
 
-def rel_l2(a, b):
-    a = np.asarray(a, np.float64)
-    b = np.asarray(b, np.float64)
-    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+TOL = (X_TOL, DELTA_TOL, KV_TOL)
 
 
-def host(t):
-    torch.cuda.synchronize()
-    return t.cpu().numpy()
-
-
-class DeviceRun:
-    """Prefill + one step of a workload on the GPU with per-block outputs."""
-
-    def __init__(self, w, layers=None, keep_prefill_x=True):
-        self.w = w
-        self.dw = D.DeviceWorkload(w, layers=layers)
-        H, L = w.dim, w.layers
-        self.xpre = [torch.full((L, c.lp, H), float("nan"), device="cuda") if keep_prefill_x else None
-                     for c in self.dw.caches]
-        self.dw.prefill_all(x_layers=self.xpre)
-        n = w.n_target
-        self.xl = torch.full((L, w.nseq * n, H), float("nan"), device="cuda")
-        self.out = self.dw.step(x_layers=self.xl)
-        torch.cuda.synchronize()
-        assert q.device_status() == 0
-
-    def kv(self, s, layer):
-        return self.dw.caches[s].layer_tensor(layer)
-
-    def step_x(self, layer, s, rows=None):
-        n = self.w.n_target
-        t = self.xl[layer, s * n:(s + 1) * n]
-        if rows is not None:
-            t = t[torch.as_tensor(rows, device="cuda")]
-        return host(t)
-
-    def step_in(self, layer, s, rows=None):
-        if layer == 0:
-            x = S.x_target(self.w)
-            return x if rows is None else x[rows]
-        return self.step_x(layer - 1, s, rows)
-
-    def pre_x(self, layer, s):
-        return host(self.xpre[s][layer])
-
-    def pre_in(self, layer, s):
-        return S.x_prefix(self.w, s) if layer == 0 else self.pre_x(layer - 1, s)
-
-
-def _check_block(got_out, x_in, ref_out, what):
-    e = rel_l2(got_out, ref_out)
-    assert e <= X_TOL, f"{what}: rel L2 {e:.3e}"
-    d = rel_l2(np.asarray(got_out, np.float64) - x_in, np.asarray(ref_out, np.float64) - x_in)
-    assert d <= DELTA_TOL, f"{what}: block delta rel L2 {d:.3e}"
-    return e, d
-
-
-def _teacher_forced_layer(run, layer, s, weights, cfg, rows_pre=None, rows_step=None):
-    """Oracle block `layer` on the GPU's inputs: prefill (K/V and output) and
-    step (output), optionally on sampled rows."""
-    w = run.w
-    segs = w.segs(s)
-    lp = O.prefix_len(segs)
-    pos = O.positions(segs)
-    cp, sp = O.rope_tables(pos[:lp], cfg["axes"], cfg["theta"])
-    vis = O.prefix_visibility(segs)
-    W = weights
-    # prefill: this layer's K/V from the GPU's prefix input of the layer
-    xin = run.pre_in(layer, s)
-    xo, k, v = O.block(xin, W, S.mods0(w), cp, sp, cfg, None, vis, rows=rows_pre)
-    kv = host(run.kv(s, layer)).astype(np.float64)
-    H = w.dim
-    ek = rel_l2(kv[:, :H], k)
-    ev = rel_l2(kv[:, H:], v)
-    assert ek <= KV_TOL and ev <= KV_TOL, f"layer {layer} seq {s}: cache K {ek:.2e} V {ev:.2e}"
-    if layer + 1 < w.layers:
-        got = run.pre_x(layer, s)
-        if rows_pre is not None:
-            got = got[rows_pre]
-            xin_r = xin[rows_pre]
-        else:
-            xin_r = xin
-        _check_block(got, xin_r, xo, f"prefill layer {layer} seq {s}")
-    # step: the GPU's input of the layer against the GPU's cache of the layer
-    ct, st = O.target_rope(segs, cfg["axes"], cfg["theta"])
-    x_in = run.step_in(layer, s)
-    ref, _, _ = O.block(x_in, W, S.mods_t(w), ct, st, cfg, (kv[:, :H], kv[:, H:]), None, rows=rows_step)
-    got = run.step_x(layer, s, rows_step)
-    x_in_r = x_in if rows_step is None else x_in[rows_step]
-    return _check_block(got, x_in_r, ref, f"step layer {layer} seq {s}")
+def _teacher_forced_layer(run, layer, s, W, cfg, rows_pre=None, rows_step=None):
+    return teacher_forced_layer(run, layer, s, W, cfg, TOL, rows_pre=rows_pre, rows_step=rows_step)
 
 
 SMALL = ["tiny_block_d256", "chain32_d256_mixed", "ragged_d512", "cfg_pair_d256", "single_row_d256"]
@@ -132,22 +47,8 @@ def test_small_workload_end_to_end_and_teacher_forced(name):
     run = DeviceRun(w)
     cfg = O.cfg_of(w)
     weights = [S.layer_weights(w, l) for l in range(w.layers)]
+    end_to_end(run, weights, cfg, TOL)
     for s in range(w.nseq):
-        segs = w.segs(s)
-        cache, xs_pre = O.prefill(S.x_prefix(w, s), weights, S.mods0(w), segs, cfg, keep_x=True)
-        x_ref, xs = O.step(S.x_target(w), weights, S.mods_t(w), segs, cache, cfg, keep_x=True)
-        # end to end: every block output of the step, every layer's cache
-        x_in = S.x_target(w)
-        for l in range(w.layers):
-            _check_block(run.step_x(l, s), x_in, xs[l], f"{name} e2e step layer {l} seq {s}")
-            x_in = xs[l]
-            kv = host(run.kv(s, l)).astype(np.float64)
-            H = w.dim
-            assert rel_l2(kv[:, :H], cache[l][0]) <= KV_TOL
-            assert rel_l2(kv[:, H:], cache[l][1]) <= KV_TOL
-        n = w.n_target
-        np.testing.assert_array_equal(host(run.out[s * n:(s + 1) * n]), run.step_x(w.layers - 1, s))
-        # teacher-forced, every layer
         for l in range(w.layers):
             _teacher_forced_layer(run, l, s, weights[l], cfg)
 
@@ -204,11 +105,7 @@ def test_step_rejects_unfilled_cache_and_small_workspace():
 
 # ------------------------------------------------------------ full width ----
 
-def _sample_rows(n, seed):
-    rng = np.random.default_rng(seed)
-    fixed = [0, 1, 2, 17, 18, 19, 126, 127, 128, 129, n // 2, n - 129, n - 128, n - 2, n - 1]
-    rnd = rng.choice(n, size=min(n, 48), replace=False).tolist()
-    return np.array(sorted(set(r for r in fixed + rnd if 0 <= r < n)), dtype=np.int64)
+_sample_rows = sample_rows
 
 
 def test_block_d4096_n4096_sampled():
@@ -252,3 +149,29 @@ def test_full_width_32_layers_sampled(name, layers_checked, layers32):
     assert np.all(np.isfinite(out))
     del run
     torch.cuda.empty_cache()
+
+
+def test_a_bad_later_layer_enqueues_nothing():
+    # every layer is validated and every tensor map encoded before the first
+    # launch: a misaligned plane in layer 3 of 32 is refused with no kernel
+    # launched and the output untouched
+    import ctypes as C
+
+    from diffusion_transformer_denoiser_qi21_gb300 import _binding as B
+    w = S.WORKLOADS["chain32_d256_mixed"]
+    dw = D.DeviceWorkload(w)
+    dw.prefill_all()
+    torch.cuda.synchronize()
+    arr = (B.Layer * w.layers)()
+    for i, l in enumerate(dw.layers):
+        arr[i] = l.c
+    arr[3].w13 = arr[3].w13 + 2  # 2-byte aligned
+    out = torch.full_like(dw.x_target, float("nan"))
+    _, before = q.profile_read()
+    rc = q.load().qi21_step(C.byref(dw.g), arr, dw.caches[0].handle, dw.x_target.data_ptr(), out.data_ptr(),
+                            dw.mods_t.data_ptr(), None, dw.ws.data_ptr(), dw.ws.numel(), None)
+    assert rc == -1 and b"layer 3" in q.load().qi21_last_error()
+    torch.cuda.synchronize()
+    _, after = q.profile_read()
+    assert after == before
+    assert torch.isnan(out).all()

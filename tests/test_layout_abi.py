@@ -81,6 +81,8 @@ def test_layout_errors(segs, code):
     (dict(dim=256, heads=2, mlp_hidden=768, layers=0), -3),
     (dict(dim=256, heads=2, mlp_hidden=768, layers=1, axes=(16, 56, 58)), -3),
     (dict(dim=256, heads=2, mlp_hidden=768, layers=1, axes=(15, 57, 56)), -3),
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=1, dtype=2), -3),
+    (dict(dim=256, heads=2, mlp_hidden=768, layers=1, dtype=-1), -3),
 ])
 def test_geometry_errors(kw, code):
     g = q.geom(**kw)
@@ -88,8 +90,9 @@ def test_geometry_errors(kw, code):
     assert q.workspace_bytes(g, 10) == 0
 
 
-def test_geometry_ok_and_sizes():
-    g = q.geom(4096, 32, 12288, 32)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_geometry_ok_and_sizes(dtype):
+    g = q.geom(4096, 32, 12288, 32, dtype=dtype)
     assert q.load().qi21_geom_check(C.byref(g)) == 0
     H, I = 4096, 12288
     assert q.layer_plane_bytes(g) == 2 * (3 * H * H + H * H + 2 * I * H + H * I)
@@ -105,10 +108,27 @@ def test_device_entry_points_reject_bad_args_before_touching_the_device():
     # null cache / pointers -> ARG, nothing enqueued (no CUDA context needed)
     assert lib.qi21_prefill(C.byref(g), None, None, None, None, None, None, 0, None) == -1
     assert lib.qi21_step(C.byref(g), None, None, None, None, None, None, None, 0, None) == -1
-    assert lib.qi21_op_gemm(0, 128, 100, 64, 8, 8, 8, 128, None, None) == -2  # N % 128
-    assert lib.qi21_op_gemm(9, 128, 128, 64, 8, 8, 8, 128, None, None) == -1  # epilogue
-    assert lib.qi21_op_rowop(4, 6, 1e-6, 8, None, None, 8, 8, None) == -2    # dim % 4
-    assert lib.qi21_op_attention(10, 2, 8, None, 0, 5, None, 8, None) == -2  # nq > own rows
+    for dt in (0, 1):
+        assert lib.qi21_op_gemm(dt, 0, 128, 100, 64, 8, 8, 8, 128, None, None) == -2  # N % 128
+        assert lib.qi21_op_gemm(dt, 9, 128, 128, 64, 8, 8, 8, 128, None, None) == -1  # epilogue
+        assert lib.qi21_op_rowop(dt, 4, 6, 1e-6, 8, None, None, 8, 8, None) == -2    # dim % 4
+        assert lib.qi21_op_attention(dt, 10, 2, 8, None, 0, 5, None, 8, None) == -2  # nq > own rows
+    # an unknown 16-bit type
+    assert lib.qi21_op_gemm(5, 0, 128, 128, 64, 8, 8, 8, 128, None, None) == -1
+    assert lib.qi21_op_rowop(-1, 4, 8, 1e-6, 8, None, None, 8, 8, None) == -1
+    assert lib.qi21_op_attention(2, 1, 2, 8, None, 0, 5, None, 8, None) == -1
+    assert lib.qi21_op_qkrope(3, 1, 2, 1e-6, 8, 8, 8, 8, 8, None) == -1
     bad = q.geom(256, 2, 768, 1, head_dim=64)
     assert lib.qi21_prefill(C.byref(bad), None, None, None, None, None, None, 0, None) == -3
     assert b"head_dim" in lib.qi21_last_error()
+    # the FP8 variant takes f16 geometries only
+    gb = q.geom(256, 2, 768, 1, dtype="bf16")
+    assert lib.qi21_layer_fp8_bytes(C.byref(gb)) == 0
+    assert lib.qi21_workspace_bytes_fp8(C.byref(gb), 16) == 0
+    assert lib.qi21_prefill_fp8(C.byref(gb), None, None, None, None, None, None, 0, None) == -3
+    assert b"FP8" in lib.qi21_last_error()
+    assert lib.qi21_layer_fp8_bytes(C.byref(g)) > 0
+    # the finite scan's element types
+    out = C.c_uint64(0)
+    assert lib.qi21_count_nonfinite(None, 0, 8, C.byref(out), None) == -1
+    assert lib.qi21_count_nonfinite(None, 0, 1, C.byref(out), None) == -1
