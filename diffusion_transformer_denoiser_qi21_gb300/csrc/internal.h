@@ -158,9 +158,10 @@ struct AttnArgs {
   int max_ctas;
 };
 
-// Most persistent attention CTAs with a split (merge flags: 2 per CTA).
+// Most persistent attention CTAs with a split (merge flags: one per query
+// row of the two 128-row tiles, per CTA boundary).
 constexpr int kMaxAttnCtas = 512;
-constexpr size_t kAttnFlagBytes = 2 * kMaxAttnCtas * sizeof(int);
+constexpr size_t kAttnFlagBytes = static_cast<size_t>(kMaxAttnCtas) * 2 * 128 * sizeof(int);
 // Bytes of split partials for `ctas` CTAs.
 size_t attn_split_bytes(int ctas);
 
@@ -187,7 +188,7 @@ struct AttnTcParams {
   int split;        // stream-K over the key blocks of all items
   long long units;  // total key blocks (split)
   float* part;      // split partials
-  int* flags;       // split merge flags [2 per CTA boundary]
+  int* flags;       // split merge flags [CTA boundary][tile][row]
   AttnTcSeq seq[kMaxSeq];
 };
 
