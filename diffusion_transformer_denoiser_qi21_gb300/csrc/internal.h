@@ -158,10 +158,9 @@ struct AttnArgs {
   int max_ctas;
 };
 
-// Most persistent attention CTAs with a split (merge flags: one per query
-// row of the two 128-row tiles, per CTA boundary).
+// Most persistent attention CTAs with a split (merge flags: 2 per CTA).
 constexpr int kMaxAttnCtas = 512;
-constexpr size_t kAttnFlagBytes = static_cast<size_t>(kMaxAttnCtas) * 2 * 128 * sizeof(int);
+constexpr size_t kAttnFlagBytes = 2 * kMaxAttnCtas * sizeof(int);
 // Bytes of split partials for `ctas` CTAs.
 size_t attn_split_bytes(int ctas);
 
@@ -188,7 +187,7 @@ struct AttnTcParams {
   int split;        // stream-K over the key blocks of all items
   long long units;  // total key blocks (split)
   float* part;      // split partials
-  int* flags;       // split merge flags [CTA boundary][tile][row]
+  int* flags;       // split merge flags [2 per CTA boundary]
   AttnTcSeq seq[kMaxSeq];
 };
 

@@ -111,10 +111,9 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// A bounded wait whose outcome is the same on every lane of the warp (the
-// tcgen05 loads and stores that follow are warp-collective).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned int* status) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+// Named barrier of the 128 threads of one softmax stage.
+__device__ __forceinline__ void stage_sync(int q) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(128) : "memory");
 }
 
 // key index of virtual key v (cache keys, padding, then own keys), or a
@@ -228,6 +227,7 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
   uint64_t* mdone = bars + 22;   // MMAs drained (give-up path)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* second = reinterpret_cast<volatile int*>(tslot + 2);  // [2] merge order of a split item
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 23; ++i) mbar_init(&bars[i], (i >= 16 && i < 18) || (i >= 20 && i < 22) ? 128 : 1);
@@ -412,7 +412,7 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const long long gb = g + j;
-        if (!warp_wait(&sfull[q], static_cast<uint32_t>(gb & 1), abort_flag, &s_attn_status)) {
+        if (!mbar_wait(&sfull[q], static_cast<uint32_t>(gb & 1), abort_flag, &s_attn_status)) {
           ok = false;
           break;
         }
@@ -500,7 +500,7 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
       if (!ok) break;
       // the item's O_q: read it, release the accumulator, write the result
       const long long gl = g + n - 1;
-      if (!warp_wait(&pvdone[q], static_cast<uint32_t>(gl & 1), abort_flag, &s_attn_status)) {
+      if (!mbar_wait(&pvdone[q], static_cast<uint32_t>(gl & 1), abort_flag, &s_attn_status)) {
         ok = false;
         break;
       }
@@ -528,10 +528,9 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
                   pack2<BF>(__uint_as_float(o[cc][8 * gq + 6]) * inv, __uint_as_float(o[cc][8 * gq + 7]) * inv));
         }
       } else {
-        // one part of a split item: store this row's partial (O
-        // transposed so that a warp's rows are contiguous, the max and the
-        // sum); the part whose row finishes second merges both rows and
-        // writes the result (rows are independent: one flag per row)
+        // one part of a split item: store the partial (O transposed so
+        // that the warp's rows are contiguous, the max and the sum); the
+        // part that finishes second merges both and writes the result
         float* mine = p.part + (static_cast<size_t>(s.slot * 2 + s.part) * 2 + q) * kPartFloats;
         const float* other = p.part + (static_cast<size_t>(s.slot * 2 + (s.part ^ 1)) * 2 + q) * kPartFloats;
 #pragma unroll
@@ -541,8 +540,11 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
         __stcg(mine + kAQ * kAD + r, m);
         __stcg(mine + kAQ * kAD + kAQ + r, l);
         __threadfence();
-        int* flag = p.flags + (s.slot * 2 + q) * kAQ + r;
-        if (atomicAdd(flag, 1) == 1) {
+        stage_sync(q);
+        int* flag = p.flags + s.slot * 2 + q;
+        if (r == 0) second[q] = atomicAdd(flag, 1);
+        stage_sync(q);
+        if (second[q] == 1) {
           __threadfence();
           const float m2 = __ldcg(other + kAQ * kAD + r);
           const float l2 = __ldcg(other + kAQ * kAD + kAQ + r);
@@ -568,8 +570,10 @@ __global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ AttnTcPa
                 dst[cc * 4 + gq] = make_uint4(w[0], w[1], w[2], w[3]);
               }
           }
-          *flag = 0;  // both parts of this row have arrived: ready for the next launch
+          if (r == 0) *flag = 0;  // both parts have arrived: ready for the next launch
         }
+        // the merge-order word is reused by this stage's next split item
+        stage_sync(q);
       }
       g += n;
     }

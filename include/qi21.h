@@ -264,7 +264,7 @@ int qi21_denoise(const qi21_geom* g, const qi21_layer* layers, const qi21_kvcach
 
 /* Size of the static device scratch behind qi21_step_noalloc: 32 MiB,
  * i.e. qi21_workspace_bytes(g, n) <= this bound (dim 4096 / mlp 12288: up to
- * 402 target rows; dim 256 / mlp 768: up to 6450). */
+ * 408 target rows; dim 256 / mlp 768: up to 6552). */
 #define QI21_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* qi21_step without a caller workspace, for callers that cannot allocate
@@ -542,7 +542,7 @@ int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void*
  * gpu_wgpu/qi21.rs, qi_flash). scratch (device, 256-byte aligned, or NULL)
  * lets a step (vis == NULL) split the queries' key blocks evenly over the
  * CTAs and merge the parts of an item cut by a CTA boundary, as the passes
- * do: its first 512 KB hold merge flags (zeroed by the call), the rest the
+ * do: its first 4 KB hold merge flags (zeroed by the call), the rest the
  * partials (about 266 KB per CTA); without it, or when it is too small,
  * each CTA takes whole 256-query items. max_ctas caps the number of
  * persistent CTAs (0 = one per SM). */

@@ -99,7 +99,7 @@ def test_geometry_ok_and_sizes(dtype):
     M = 4096
     per_row = 4 * H + 2 * H + 6 * H + 2 * H + 2 * I
     assert q.workspace_bytes(g, M) >= M * per_row + 16 * H
-    assert q.workspace_bytes(g, M) < M * per_row + 16 * H + (512 << 10) + 9 * 256  # + the attention merge flags
+    assert q.workspace_bytes(g, M) < M * per_row + 16 * H + 4096 + 9 * 256  # + the attention merge flags
 
 
 def test_device_entry_points_reject_bad_args_before_touching_the_device():
