@@ -461,17 +461,13 @@ def op_kvcopy(panel, kv, stream=None):
                                 _stream(stream)))
 
 
-def op_attention(panel, heads, out, nq, n_own, kv_pre=None, n_pre=0, vis=None, scratch=None, max_ctas=0,
-                 stream=None):
-    """qi21_op_attention; panel, kv_pre and out all f16 or all bf16; scratch
-    (a uint8 CUDA tensor) enables the split of a step's key blocks over the
-    CTAs, max_ctas caps the CTA count."""
+def op_attention(panel, heads, out, nq, n_own, kv_pre=None, n_pre=0, vis=None, stream=None):
+    """qi21_op_attention; panel, kv_pre and out all f16 or all bf16."""
     torch = _torch()
-    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
     check(load().qi21_op_attention(_dt_code(panel), nq, heads, _ptr(panel, None, "panel"),
                                    _ptr(kv_pre, panel.dtype, "kv_pre"), n_pre, n_own,
                                    _ptr(vis, torch.int32, "vis"), _ptr(out, panel.dtype, "out"),
-                                   _ptr(scratch, None, "scratch"), nbytes, int(max_ctas), _stream(stream)))
+                                   _stream(stream)))
 
 
 def selftest_wait_timeout(stream=None):

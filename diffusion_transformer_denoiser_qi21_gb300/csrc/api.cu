@@ -261,7 +261,7 @@ static int elem_of(const qi21_geom* g) { return g->dtype == QI21_DTYPE_BF16 ? QI
 static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t x, xn, panel, att, hid, md, aflags, q8, qs, total;
+  size_t x, xn, panel, att, hid, md, q8, qs, total;
 };
 
 // fp8: the E4M3 activation rows (one buffer [M][max(H, I)] shared by xn,
@@ -282,8 +282,6 @@ static WsLayout ws_layout(const qi21_geom* g, int rows, bool fp8 = false) {
   off = align256(off + M * I * 2);
   w.md = off;
   off = align256(off + 4 * H * 4);
-  w.aflags = off;  // attention merge flags (zeroed at the start of every pass)
-  off = align256(off + kAttnFlagBytes);
   w.q8 = w.qs = 0;
   if (fp8) {
     w.q8 = off;
@@ -639,8 +637,6 @@ struct PassBufs {
   void* att;    // dt [M][H]
   void* hid;    // dt [M][I]
   float* md;
-  int* aflags;       // attention merge flags
-  size_t hid_bytes;  // the hid buffer, dead during the attention: its split partials
   uint8_t* q8;  // FP8 pass: E4M3 activation rows (xn, att, hid in turn)
   float* qs;    // FP8 pass: their row scales
 };
@@ -696,10 +692,6 @@ int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8
     aa.out = b.att;
     aa.heads = g->heads;
     aa.dt = dt;
-    aa.part = b.hid;  // written by the gate/up projection only after the attention
-    aa.part_bytes = b.hid_bytes;
-    aa.flags = b.aflags;
-    aa.max_ctas = 0;
     if (prefill) {
       aa.nseq = 1;
       aa.seq[0] = AttnSeq{nullptr, 0, 0, M, 0, M, pcache->vis};
@@ -764,8 +756,6 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
     return QI21_OK;
   };
   int rc;
-  // the attention's merge flags start at zero (each launch leaves them so)
-  QI21_CK(cudaMemsetAsync(b.aflags, 0, kAttnFlagBytes, s), "attention flags");
   if ((rc = ln(s1)) != QI21_OK) return rc;
   for (int l = 0; l < L; ++l) {
     const LayerRange range(prefill, l);
@@ -823,9 +813,7 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, b
   b->panel = base + w.panel;
   b->att = base + w.att;
   b->hid = base + w.hid;
-  b->hid_bytes = static_cast<size_t>(M) * g->mlp_hidden * 2;
   b->md = reinterpret_cast<float*>(base + w.md);
-  b->aflags = reinterpret_cast<int*>(base + w.aflags);
   b->q8 = fp8 ? base + w.q8 : nullptr;
   b->qs = fp8 ? reinterpret_cast<float*>(base + w.qs) : nullptr;
   return QI21_OK;
@@ -1304,13 +1292,9 @@ int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void*
 }
 
 int qi21_op_attention(int32_t dtype, int32_t nq, int32_t heads, const void* panel, const void* kv_pre, int32_t n_pre,
-                      int32_t n_own, const uint32_t* vis, void* out, void* scratch, size_t scratch_bytes,
-                      int32_t max_ctas, void* stream) {
+                      int32_t n_own, const uint32_t* vis, void* out, void* stream) {
   if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
-  if (nq < 0 || heads <= 0 || n_pre < 0 || n_own < 0 || max_ctas < 0) return fail(QI21_ERR_SHAPE, "bad sizes");
-  if (scratch != nullptr && (reinterpret_cast<uintptr_t>(scratch) % 256 || scratch_bytes < kAttnFlagBytes))
-    return fail(QI21_ERR_WORKSPACE, "attention scratch must be 256-byte aligned and hold at least %zu bytes",
-                kAttnFlagBytes);
+  if (nq < 0 || heads <= 0 || n_pre < 0 || n_own < 0) return fail(QI21_ERR_SHAPE, "bad sizes");
   if (nq > n_own) return fail(QI21_ERR_SHAPE, "nq %d > own rows %d (queries are panel rows)", nq, n_own);
   if (nq == 0) return QI21_OK;
   if (!panel || !out || (n_pre > 0 && !kv_pre)) return fail(QI21_ERR_ARG, "null pointer");
@@ -1322,17 +1306,7 @@ int qi21_op_attention(int32_t dtype, int32_t nq, int32_t heads, const void* pane
   a.dt = dtype;
   a.nseq = 1;
   a.seq[0] = AttnSeq{kv_pre, n_pre, 0, nq, 0, n_own, vis};
-  a.max_ctas = max_ctas;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  AttnPlan plan;
-  if (scratch != nullptr) {
-    a.flags = static_cast<int*>(scratch);
-    a.part = static_cast<uint8_t*>(scratch) + kAttnFlagBytes;
-    a.part_bytes = scratch_bytes - kAttnFlagBytes;
-  }
-  QI21_CK(make_attn_plan(a, &plan), "attention plan");
-  if (scratch != nullptr) QI21_CK(cudaMemsetAsync(scratch, 0, kAttnFlagBytes, s), "attention flags");
-  QI21_CK(launch_attn_plan(plan, s), "attention");
+  QI21_CK(launch_attention(a, static_cast<cudaStream_t>(stream)), "attention");
   return QI21_OK;
 }
 

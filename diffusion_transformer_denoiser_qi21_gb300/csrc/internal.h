@@ -148,31 +148,13 @@ struct AttnArgs {
   int dt;
   int nseq;
   AttnSeq seq[kMaxSeq];
-  // stream-K split of a step (optional): partials scratch (device,
-  // attn_split_bytes(ctas)) and merge flags (device, zero before the first
-  // launch; each launch leaves them zero), and a cap on the CTA count (0 =
-  // one per SM)
-  void* part;
-  size_t part_bytes;
-  int* flags;
-  int max_ctas;
 };
-
-// Most persistent attention CTAs with a split (merge flags: 2 per CTA).
-constexpr int kMaxAttnCtas = 512;
-constexpr size_t kAttnFlagBytes = 2 * kMaxAttnCtas * sizeof(int);
-// Bytes of split partials for `ctas` CTAs.
-size_t attn_split_bytes(int ctas);
 
 // Kernel parameters of one attention launch (tensor maps encoded).
 struct AttnTcSeq {
   CUtensorMap kvmap;  // cache [n_pre][2H], box 64 x 64 (unused if n_pre == 0)
   const uint32_t* vis;
   int n_pre, pad_end, q_row0, nq, own_row0, n_own;
-  int pairs;        // 256-query items per head
-  int nkb;          // key blocks per item in a step (0: from vis per item)
-  int item0;        // first item of this sequence
-  long long unit0;  // first key-block unit of this sequence (split)
 };
 
 struct AttnTcParams {
@@ -180,14 +162,7 @@ struct AttnTcParams {
   CUtensorMap panel_kv;  // same, box 64 x 64 (K, V)
   void* out;
   int H;
-  int nseq;
   float scale_log2;
-  int G;            // persistent CTAs
-  int items;        // work items (sequence, head, 256-query pair)
-  int split;        // stream-K over the key blocks of all items
-  long long units;  // total key blocks (split)
-  float* part;      // split partials
-  int* flags;       // split merge flags [2 per CTA boundary]
   AttnTcSeq seq[kMaxSeq];
 };
 

@@ -539,17 +539,10 @@ int qi21_op_kvcopy(int32_t rows, int32_t dim, const void* panel, void* kv, void*
  * (K at columns [H, 2H), V at [2H, 3H)). Query i sees keys [0, vis[i]) if
  * vis != NULL (uint32 [nq], non-decreasing, >= 1), else all n_pre + n_own
  * keys. out T [nq][H] (qwen_image21.rs, Qi21Dit::attention;
- * gpu_wgpu/qi21.rs, qi_flash). scratch (device, 256-byte aligned, or NULL)
- * lets a step (vis == NULL) split the queries' key blocks evenly over the
- * CTAs and merge the parts of an item cut by a CTA boundary, as the passes
- * do: its first 4 KB hold merge flags (zeroed by the call), the rest the
- * partials (about 266 KB per CTA); without it, or when it is too small,
- * each CTA takes whole 256-query items. max_ctas caps the number of
- * persistent CTAs (0 = one per SM). */
+ * gpu_wgpu/qi21.rs, qi_flash). */
 int qi21_op_attention(int32_t dtype, int32_t nq, int32_t heads, const void* panel,
                       const void* kv_pre, int32_t n_pre, int32_t n_own, const uint32_t* vis,
-                      void* out, void* scratch, size_t scratch_bytes, int32_t max_ctas,
-                      void* stream);
+                      void* out, void* stream);
 
 #ifdef __cplusplus
 }

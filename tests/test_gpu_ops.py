@@ -201,14 +201,13 @@ def test_gemm_full_width_sampled_rows():
 
 # ------------------------------------------------------------- attention ----
 
-def _attn_case(case, heads, nq, n_own, n_pre, vis=None, scratch=None, max_ctas=0):
+def _attn_case(case, heads, nq, n_own, n_pre, vis=None):
     H = heads * 128
     panel = S.op_tensor(9, case, 0, (n_own, 3 * H), 1.0).astype(np.float16)
     kvp = S.op_tensor(9, case, 1, (max(n_pre, 1), 2 * H), 1.0).astype(np.float16)[:n_pre]
     out = torch.full((nq, H), float("nan"), dtype=torch.float16, device="cuda")
     visd = None if vis is None else T(np.asarray(vis, np.int32))
-    q.op_attention(T(panel), heads, out, nq, n_own, kv_pre=T(kvp) if n_pre else None, n_pre=n_pre, vis=visd,
-                   scratch=scratch, max_ctas=max_ctas)
+    q.op_attention(T(panel), heads, out, nq, n_own, kv_pre=T(kvp) if n_pre else None, n_pre=n_pre, vis=visd)
     p = panel.astype(np.float64)
     kv = kvp.astype(np.float64)
     K = np.concatenate([kv[:, :H], p[:, H:2 * H]], axis=0)
@@ -235,28 +234,6 @@ def test_attention_step_mode(heads, nq, n_own, n_pre):
     assert np.all(np.isfinite(got))
     assert rel_l2(got, ref) < 2e-3
     assert np.max(np.abs(got - ref)) < 1e-2
-
-
-# the persistent CTAs split a step's key blocks evenly (stream-K) and merge
-# the two parts of an item cut by a CTA boundary: few CTAs force many cuts,
-# at every kind of position (within the cache, in the panel, ragged tiles)
-@pytest.mark.parametrize("heads,nq,n_pre,ctas", [
-    (2, 1000, 70, 5),     # 8 items of 9 blocks over 5 CTAs
-    (2, 1000, 70, 7),
-    (3, 300, 4114, 4),    # long cache: cuts fall inside the cache part
-    (1, 1537, 1, 3),      # a ragged last pair (one live row in its first tile)
-    (32, 512, 18, 152),   # 64 items over up to 152 CTAs: no split (fewer items than CTAs)
-    (12, 4096, 18, 0),    # one CTA per SM: 192 items of 33 blocks, the full-width query count
-])
-def test_attention_split_step_mode(heads, nq, n_pre, ctas):
-    scratch = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
-    got, ref = _attn_case(nq * 7 + n_pre, heads, nq, nq, n_pre, scratch=scratch, max_ctas=ctas)
-    assert np.all(np.isfinite(got))
-    assert rel_l2(got, ref) < 2e-3
-    assert np.max(np.abs(got - ref)) < 1e-2
-    # the merge flags are left at zero: a second call gives the same bits
-    got2, _ = _attn_case(nq * 7 + n_pre, heads, nq, nq, n_pre, scratch=scratch, max_ctas=ctas)
-    np.testing.assert_array_equal(got2, got)
 
 
 @pytest.mark.parametrize("segs", [

@@ -99,7 +99,7 @@ def test_geometry_ok_and_sizes(dtype):
     M = 4096
     per_row = 4 * H + 2 * H + 6 * H + 2 * H + 2 * I
     assert q.workspace_bytes(g, M) >= M * per_row + 16 * H
-    assert q.workspace_bytes(g, M) < M * per_row + 16 * H + 4096 + 9 * 256  # + the attention merge flags
+    assert q.workspace_bytes(g, M) < M * per_row + 16 * H + 8 * 256
 
 
 def test_device_entry_points_reject_bad_args_before_touching_the_device():
@@ -112,11 +112,11 @@ def test_device_entry_points_reject_bad_args_before_touching_the_device():
         assert lib.qi21_op_gemm(dt, 0, 128, 100, 64, 8, 8, 8, 128, None, None) == -2  # N % 128
         assert lib.qi21_op_gemm(dt, 9, 128, 128, 64, 8, 8, 8, 128, None, None) == -1  # epilogue
         assert lib.qi21_op_rowop(dt, 4, 6, 1e-6, 8, None, None, 8, 8, None) == -2    # dim % 4
-        assert lib.qi21_op_attention(dt, 10, 2, 8, None, 0, 5, None, 8, None, 0, 0, None) == -2  # nq > own rows
+        assert lib.qi21_op_attention(dt, 10, 2, 8, None, 0, 5, None, 8, None) == -2  # nq > own rows
     # an unknown 16-bit type
     assert lib.qi21_op_gemm(5, 0, 128, 128, 64, 8, 8, 8, 128, None, None) == -1
     assert lib.qi21_op_rowop(-1, 4, 8, 1e-6, 8, None, None, 8, 8, None) == -1
-    assert lib.qi21_op_attention(2, 1, 2, 8, None, 0, 5, None, 8, None, 0, 0, None) == -1
+    assert lib.qi21_op_attention(2, 1, 2, 8, None, 0, 5, None, 8, None) == -1
     assert lib.qi21_op_qkrope(3, 1, 2, 1e-6, 8, 8, 8, 8, 8, None) == -1
     bad = q.geom(256, 2, 768, 1, head_dim=64)
     assert lib.qi21_prefill(C.byref(bad), None, None, None, None, None, None, 0, None) == -3
