@@ -645,7 +645,7 @@ struct PassBufs {
 struct LayerPlan {
   GemmPlan pq, po, p13, p2;
   AttnPlan at;
-  void* kv;       // prefill: the layer's cache block (the K|V copy target)
+  void* kv;       // prefill: the layer's cache block (written by the qkv epilogue)
   bool has_attn;  // false for the prefill's last layer (stops after its cache write)
 };
 
@@ -674,16 +674,19 @@ int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8
     const bool last = (l + 1 == L);
     const float* norm_q = f8 ? l8[l].norm_q : layers[l].norm_q;
     const float* norm_k = f8 ? l8[l].norm_k : layers[l].norm_k;
-    // qkv projection with the qk RMSNorm + RoPE fused into its epilogue
+    // qkv projection with the qk RMSNorm + RoPE fused into its epilogue (and,
+    // in a prefill, the layer's K|V cache rows written by the same store)
+    const int epi_qkv = prefill ? EPI_QKV_KV : EPI_QKV;
     if (f8)
-      QI21_CK(make_gemm_plan_f8(&lp.pq, EPI_QKV, M, 3 * H, H, b.q8, b.qs, l8[l].wqkv, l8[l].s_qkv, b.panel, 3 * H,
+      QI21_CK(make_gemm_plan_f8(&lp.pq, epi_qkv, M, 3 * H, H, b.q8, b.qs, l8[l].wqkv, l8[l].s_qkv, b.panel, 3 * H,
                                 nullptr),
               "qkv plan");
     else
-      QI21_CK(make_gemm_plan(&lp.pq, EPI_QKV, dt, M, 3 * H, H, b.xn, layers[l].wqkv, b.panel, 3 * H, nullptr),
+      QI21_CK(make_gemm_plan(&lp.pq, epi_qkv, dt, M, 3 * H, H, b.xn, layers[l].wqkv, b.panel, 3 * H, nullptr),
               "qkv plan");
-    lp.pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs};
     lp.kv = prefill ? static_cast<uint16_t*>(pcache->kv) + static_cast<size_t>(l) * pcache->lp * 2 * H : nullptr;
+    // a prefill's K|V cache rows are written by the qkv epilogue itself
+    lp.pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs, lp.kv};
     lp.has_attn = !(prefill && last);
     if (!lp.has_attn) break;
     AttnArgs aa{};
@@ -764,10 +767,6 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
     {
       ProfScope ps(QI21_CLASS_QKV, s);
       QI21_CK(launch_gemm(lp.pq, s), "qkv gemm");
-    }
-    if (prefill) {
-      ProfScope ps(QI21_CLASS_KVCOPY, s);
-      QI21_CK(launch_kvcopy(M, H, b.panel, lp.kv, s), "kvcopy");
     }
     if (!lp.has_attn) break;
     {

@@ -91,7 +91,7 @@ cudaError_t launch_final(int n, int dim, float eps, const float* x, const float*
 
 // ------------------------------------------------------------------ GEMM ----
 
-enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4 };
+enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_QKV_KV = 5 };
 
 // Extra inputs of the EPI_QKV epilogue: per-head RMSNorm weights of q and k,
 // epsilon, the model width and the RoPE tables of the rows.
@@ -101,6 +101,7 @@ struct QkvEpi {
   float eps;
   int H;
   RopeTables tabs;
+  void* kv;  // EPI_QKV_KV (prefill): the layer's cache block [M][2H] (K then V), also written
 };
 
 struct GemmPlan {

@@ -13,6 +13,9 @@
 //              interleaved RoPE applied to the q and k columns on the way out
 //              (qwen_image21.rs, Qi21Dit::qk_norm_rope; each thread holds
 //              whole 128-column head vectors of its row)
+//   EPI_QKV_KV the same, the k and v columns also stored into the layer's
+//              K|V cache rows (a prefill; gpu_wgpu/qi21.rs, qi_kvcopy, folded
+//              into the store)
 //   EPI_F32    plain f32 store (single-operation checks)
 //
 // The FP8 instance (OP = kOpF8) runs the same pipeline on E4M3 operands:
@@ -154,7 +157,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
         }
       }
     }
-  } else if constexpr (EPI == EPI_QKV) {
+  } else if constexpr (EPI == EPI_QKV || EPI == EPI_QKV_KV) {
     const QkvEpi& qe = ep.qkv;
     uint16_t* out = static_cast<uint16_t*>(ep.out) + static_cast<size_t>(row) * ep.ldo;
     // this row's RoPE table (the sequence whose rows contain it)
@@ -178,16 +181,24 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 #pragma unroll
       for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
       uint4* dst = reinterpret_cast<uint4*>(out + col);
+      // prefill: the same k / v values into the cache row (K at col - H, V at col - H)
+      uint4* kvd = (EPI == EPI_QKV_KV && part > 0)
+                       ? reinterpret_cast<uint4*>(static_cast<uint16_t*>(qe.kv) +
+                                                  static_cast<size_t>(row) * 2 * qe.H + (col - qe.H))
+                       : nullptr;
       if (part == 2) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[c * 4 + j] = make_uint4(
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = make_uint4(
                 pack2<BF>(__uint_as_float(r[c][8 * j + 0]), __uint_as_float(r[c][8 * j + 1])),
                 pack2<BF>(__uint_as_float(r[c][8 * j + 2]), __uint_as_float(r[c][8 * j + 3])),
                 pack2<BF>(__uint_as_float(r[c][8 * j + 4]), __uint_as_float(r[c][8 * j + 5])),
                 pack2<BF>(__uint_as_float(r[c][8 * j + 6]), __uint_as_float(r[c][8 * j + 7])));
+            dst[c * 4 + j] = v;
+            if constexpr (EPI == EPI_QKV_KV) kvd[c * 4 + j] = v;
+          }
         continue;
       }
       float ss[4] = {0.f, 0.f, 0.f, 0.f};
@@ -217,10 +228,13 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
           const float b2 = __uint_as_float(r[c][8 * j + 5]) * inv * wb.y;
           const float a3 = __uint_as_float(r[c][8 * j + 6]) * inv * wb.z;
           const float b3 = __uint_as_float(r[c][8 * j + 7]) * inv * wb.w;
-          dst[c * 4 + j] = make_uint4(pack2<BF>(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
-                                      pack2<BF>(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
-                                      pack2<BF>(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
-                                      pack2<BF>(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
+          const uint4 v = make_uint4(pack2<BF>(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
+                                     pack2<BF>(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
+                                     pack2<BF>(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
+                                     pack2<BF>(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
+          dst[c * 4 + j] = v;
+          if constexpr (EPI == EPI_QKV_KV)
+            if (part == 1) kvd[c * 4 + j] = v;
         }
       }
     }
@@ -693,6 +707,7 @@ static cudaError_t launch_16(const GemmPlan& p, cudaStream_t s) {
       case EPI_RESID: return launch_t<256, EPI_RESID, OP>(p, s);
       case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, OP>(p, s);
       case EPI_QKV: return launch_t<256, EPI_QKV, OP>(p, s);
+      case EPI_QKV_KV: return launch_t<256, EPI_QKV_KV, OP>(p, s);
     }
   } else {
     switch (p.epi) {
@@ -701,6 +716,7 @@ static cudaError_t launch_16(const GemmPlan& p, cudaStream_t s) {
       case EPI_RESID: return launch_t<128, EPI_RESID, OP>(p, s);
       case EPI_SWIGLU: return launch_t<128, EPI_SWIGLU, OP>(p, s);
       case EPI_QKV: return launch_t<128, EPI_QKV, OP>(p, s);
+      case EPI_QKV_KV: return launch_t<128, EPI_QKV_KV, OP>(p, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -715,6 +731,7 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t s) {
       case EPI_RESID: return launch_t<256, EPI_RESID, kOpF8>(p, s);
       case EPI_SWIGLU: return launch_t<256, EPI_SWIGLU, kOpF8>(p, s);
       case EPI_QKV: return launch_t<256, EPI_QKV, kOpF8>(p, s);
+      case EPI_QKV_KV: return launch_t<256, EPI_QKV_KV, kOpF8>(p, s);
     }
     return cudaErrorInvalidValue;
   }

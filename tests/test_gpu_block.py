@@ -175,3 +175,24 @@ def test_a_bad_later_layer_enqueues_nothing():
     _, after = q.profile_read()
     assert after == before
     assert torch.isnan(out).all()
+
+
+@pytest.mark.parametrize("name", ["ragged_d512", "chain32_d256_mixed", "tiny_block_d256_bf16"])
+def test_prefill_cache_rows_are_the_panel_k_v_bits(name):
+    # the qkv epilogue of a prefill stores each k and v value into the panel
+    # and into the layer's cache row; the last layer stops after it, so the
+    # workspace still holds that layer's panel: its K|V columns and the cache
+    # of the last layer agree bit for bit
+    w = S.WORKLOADS[name]
+    dw = D.DeviceWorkload(w)
+    dw.prefill_all()
+    torch.cuda.synchronize()
+    H, lp = w.dim, dw.caches[0].lp
+
+    def a256(v):
+        return (v + 255) // 256 * 256
+
+    off = a256(lp * H * 4) + a256(lp * H * 2)  # x [lp][H] f32, xn [lp][H], then the panel [lp][3H]
+    panel = dw.ws[off:off + lp * 3 * H * 2].view(torch.int16).view(lp, 3 * H)
+    kv = dw.caches[0].layer_tensor(w.layers - 1).view(torch.int16)
+    assert torch.equal(kv, panel[:, H:])
