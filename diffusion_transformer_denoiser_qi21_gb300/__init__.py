@@ -20,7 +20,7 @@ __all__ = [
     "Geom", "Qi21Error", "KVCache", "geom", "layout_rows", "layout_indices", "layer_plane_bytes",
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
     "timestep_mods", "denoise", "set_checks", "PackedLayerFp8", "pack_layer_fp8", "workspace_bytes_fp8",
-    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "denoise_batch", "device_status", "selftest_wait_timeout", "build",
+    "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "CHECK_AMAX", "AMAX_SITES", "amax_read", "denoise_batch", "device_status", "selftest_wait_timeout", "build",
     "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
@@ -274,6 +274,16 @@ def graph_denoise_batch(g: Geom, layers, caches, tok, w_in, mods, final_scale, w
 
 
 CHECK_FINITE = 1
+CHECK_AMAX = 2
+AMAX_SITES = ("attn-in", "qkv", "attn-out", "ffn-in", "hidden")
+
+
+def amax_read(reset=True) -> dict:
+    """qi21_amax_read: {site: largest |value|} of the AMAX probe (synchronises)."""
+    import numpy as np
+    out = np.zeros(5, np.float32)
+    check(load().qi21_amax_read(out.ctypes.data, 1 if reset else 0))
+    return dict(zip(AMAX_SITES, out.tolist()))
 
 
 def set_checks(flags: int) -> int:

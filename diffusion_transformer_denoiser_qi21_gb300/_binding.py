@@ -83,6 +83,7 @@ _SIGS = {
     "qi21_embed": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "qi21_final": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp]),
     "qi21_set_checks": (C.c_uint32, [C.c_uint32]),
+    "qi21_amax_read": (C.c_int, [_vp, _i32]),
     "qi21_layer_fp8_bytes": (C.c_size_t, [_vp]),
     "qi21_workspace_bytes_fp8": (C.c_size_t, [_vp, _i32]),
     "qi21_pack_layer_fp8": (C.c_int, [_vp, _vp, _vp, C.c_size_t, _vp, _vp]),

@@ -629,6 +629,9 @@ int check_layers_fp8(const qi21_geom* g, const qi21_layer_fp8* layers) {
 }
 
 
+// Optional checks of qi21_set_checks (process-wide flags).
+std::atomic<uint32_t> g_checks{0};
+
 // Buffers of a pass (workspace views; x may be the caller's x_out).
 struct PassBufs {
   float* x;
@@ -741,14 +744,26 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
   const int H = g->dim, I = g->mlp_hidden, L = g->layers, dt = g->dtype;
   const float* s1 = b.md;
   const float* s2 = b.md + 2 * H;
+  // the AMAX probe (QI21_CHECK_AMAX, 16-bit passes): largest |value| of a
+  // site's rows x cols 16-bit buffer
+  const bool amax = !f8 && (g_checks.load(std::memory_order_relaxed) & QI21_CHECK_AMAX);
+  auto probe = [&](const void* buf, int cols, int ld, int site) -> int {
+    if (!amax) return QI21_OK;
+    ProfScope ps(QI21_CLASS_MISC, s);
+    QI21_CK(launch_amax(buf, static_cast<size_t>(M), static_cast<size_t>(cols), static_cast<size_t>(ld), dt, site, s),
+            "amax");
+    return QI21_OK;
+  };
   // the modulated LayerNorm of x (16-bit xn, or E4M3 rows + scales)
   auto ln = [&](const float* scale) -> int {
-    ProfScope ps(QI21_CLASS_ROWOP, s);
-    if (f8)
-      QI21_CK(launch_rowop_q8(M, H, g->eps, b.x, scale, b.q8, b.qs, s), "rowop q8");
-    else
-      QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, scale, b.xn, dt, s), "rowop");
-    return QI21_OK;
+    {
+      ProfScope ps(QI21_CLASS_ROWOP, s);
+      if (f8)
+        QI21_CK(launch_rowop_q8(M, H, g->eps, b.x, scale, b.q8, b.qs, s), "rowop q8");
+      else
+        QI21_CK(launch_rowop(M, H, g->eps, b.x, nullptr, nullptr, scale, b.xn, dt, s), "rowop");
+    }
+    return probe(b.xn, H, H, scale == s1 ? AMAX_ATTN_IN : AMAX_FFN_IN);
   };
   // f16 rows -> E4M3 rows + scales (FP8 pass: att and hid)
   auto quant = [&](const void* a, int cols) -> int {
@@ -768,11 +783,13 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
       ProfScope ps(QI21_CLASS_QKV, s);
       QI21_CK(launch_gemm(lp.pq, s), "qkv gemm");
     }
+    if ((rc = probe(b.panel, 3 * H, 3 * H, AMAX_QKV)) != QI21_OK) return rc;
     if (!lp.has_attn) break;
     {
       ProfScope ps(QI21_CLASS_ATTENTION, s);
       QI21_CK(launch_attn_plan(lp.at, s), "attention");
     }
+    if ((rc = probe(b.att, H, H, AMAX_ATTN_OUT)) != QI21_OK) return rc;
     if (f8 && (rc = quant(b.att, H)) != QI21_OK) return rc;
     {
       ProfScope ps(QI21_CLASS_O, s);
@@ -783,6 +800,7 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
       ProfScope ps(QI21_CLASS_GATEUP, s);
       QI21_CK(launch_gemm(lp.p13, s), "gate/up gemm");
     }
+    if ((rc = probe(b.hid, I, I, AMAX_HIDDEN)) != QI21_OK) return rc;
     if (f8 && (rc = quant(b.hid, I)) != QI21_OK) return rc;
     {
       ProfScope ps(QI21_CLASS_DOWN, s);
@@ -818,7 +836,6 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, b
   return QI21_OK;
 }
 
-std::atomic<uint32_t> g_checks{0};
 std::mutex g_count_mu;
 
 int count_bad(const void* x, size_t count, int eb, unsigned long long* bad, cudaStream_t s) {
@@ -895,6 +912,12 @@ int prefill_impl(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_
 extern "C" {
 
 uint32_t qi21_set_checks(uint32_t flags) { return g_checks.exchange(flags); }
+
+int qi21_amax_read(float* out, int32_t reset) {
+  if (out == nullptr) return fail(QI21_ERR_ARG, "null output");
+  QI21_CK(amax_read(out, reset != 0), "amax read");
+  return QI21_OK;
+}
 
 int qi21_count_nonfinite(const void* x, size_t count, int32_t elem_type, uint64_t* out_count, void* stream) {
   if (elem_type != QI21_ELEM_F16 && elem_type != QI21_ELEM_BF16 && elem_type != QI21_ELEM_F32)

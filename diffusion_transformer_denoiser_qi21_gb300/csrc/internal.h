@@ -89,6 +89,15 @@ cudaError_t count_nonfinite(const void* x, size_t count, int elem, unsigned long
 cudaError_t launch_final(int n, int dim, float eps, const float* x, const float* fs, const float* w_out,
                          float* out, cudaStream_t s);
 
+// AMAX probe: sites attn-in, qkv, attn-out, ffn-in, hidden. launch_amax
+// raises slot `site` to max |x| over rows x cols 16-bit values (row stride
+// ld, cols % 8 == 0, 16-byte aligned rows); amax_read synchronises the
+// device, reads the slots (and zeroes them if reset).
+constexpr int kAmaxSites = 5;
+enum AmaxSite : int { AMAX_ATTN_IN = 0, AMAX_QKV = 1, AMAX_ATTN_OUT = 2, AMAX_FFN_IN = 3, AMAX_HIDDEN = 4 };
+cudaError_t launch_amax(const void* x, size_t rows, size_t cols, size_t ld, int dt, int site, cudaStream_t s);
+cudaError_t amax_read(float* out, bool reset);
+
 // ------------------------------------------------------------------ GEMM ----
 
 enum Epi : int { EPI_F16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_QKV_KV = 5 };

@@ -7,6 +7,7 @@
 // Also the timestep conditioning (qwen_image21.rs, Qi21Dit::temb and
 // Qi21Dit::mods): matrix-vector products, bound by reading the f32 weights.
 #include <algorithm>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -326,6 +327,62 @@ cudaError_t count_nonfinite(const void* x, size_t count, int elem, unsigned long
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
   *out = h;
   return cudaSuccess;
+}
+
+// --------------------------------------------------------------- amax ----
+// Largest |value| stored at each 16-bit activation site of a pass (the
+// page's CMF_QI21_AMAX probe, gpu_wgpu/qi21.rs, AMAX_SITES): one slot per
+// site in a file-scope device array (each device has its own), raised with
+// atomicMax on the f32 bit pattern (non-negative floats order as their
+// bits; a NaN orders above every finite value and infinity).
+static __device__ unsigned int g_amax[kAmaxSites];
+
+template <bool BF>
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, size_t rows, size_t cols,
+                                                   size_t ld, int site) {
+  const size_t n8 = cols / 8;  // 16-byte groups per row
+  const size_t total = rows * n8;
+  float m = 0.f;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i / n8;
+    const uint4 u = reinterpret_cast<const uint4*>(x + r * ld)[i - r * n8];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = unpack2<BF>(w[k]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      if (f.x != f.x || f.y != f.y) m = __uint_as_float(0x7fc00000u);  // keep a NaN visible
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = __uint_as_float(max(__float_as_uint(m), __shfl_xor_sync(0xffffffffu, __float_as_uint(m), o)));
+  if ((threadIdx.x & 31) == 0) atomicMax(&g_amax[site], __float_as_uint(m));
+}
+
+cudaError_t launch_amax(const void* x, size_t rows, size_t cols, size_t ld, int dt, int site, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const size_t total = rows * (cols / 8);
+  const unsigned grid = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(sm_count()) * 8));
+  const uint16_t* p = static_cast<const uint16_t*>(x);
+  if (dt == DT_BF16)
+    amax_kernel<true><<<grid, 256, 0, s>>>(p, rows, cols, ld, site);
+  else
+    amax_kernel<false><<<grid, 256, 0, s>>>(p, rows, cols, ld, site);
+  return cudaGetLastError();
+}
+
+cudaError_t amax_read(float* out, bool reset) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  unsigned int v[kAmaxSites];
+  if ((e = cudaMemcpyFromSymbol(v, g_amax, sizeof v)) != cudaSuccess) return e;
+  memcpy(out, v, sizeof v);  // the slots hold f32 bit patterns
+  if (reset) {
+    const unsigned int z[kAmaxSites] = {};
+    e = cudaMemcpyToSymbol(g_amax, z, sizeof z);
+  }
+  return e;
 }
 
 // ---------------------------------------------------- bounded-wait test ----

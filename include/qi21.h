@@ -334,7 +334,23 @@ int qi21_timestep_mods(int32_t dim, float t, const float* t_lin1, const float* t
  * nothing synchronises. Do not set it while capturing a CUDA graph.
  * Returns the previous flags. */
 #define QI21_CHECK_FINITE 1u
+/* QI21_CHECK_AMAX is the page's AMAX probe (gpu_wgpu/qi21.rs, the
+ * CMF_QI21_AMAX sites and read_amax): with it set, every f16 / bf16 pass
+ * (prefill, step, denoiser call; not the FP8 variant) also raises, on the
+ * device, the largest |value| stored at each of five 16-bit sites over all
+ * of its layers: attn-in (the modulated LayerNorm before the qkv
+ * projection), qkv (the panel after the qk norm and RoPE), attn-out (the
+ * attention output), ffn-in (the second modulated LayerNorm) and hidden
+ * (the SwiGLU rows). One extra read of each buffer per layer; nothing
+ * synchronises. Flags are read when a pass is enqueued or recorded. */
+#define QI21_CHECK_AMAX 2u
 uint32_t qi21_set_checks(uint32_t flags);
+
+/* The five AMAX maxima of the current device, in the site order above,
+ * into out[5] (host), raised since the last reset; a NaN stored at a site
+ * reads as NaN. Synchronises the device. reset != 0 zeroes them after the
+ * read. */
+int qi21_amax_read(float* out, int32_t reset);
 
 /* Element types of qi21_count_nonfinite. */
 #define QI21_ELEM_F16 2

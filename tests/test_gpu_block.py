@@ -19,7 +19,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import diffusion_transformer_denoiser_qi21_gb300 as q  # noqa: E402
-from blockcheck import DeviceRun, end_to_end, host, sample_rows, teacher_forced_layer  # noqa: E402
+from blockcheck import DeviceRun, end_to_end, host, rel_l2, sample_rows, teacher_forced_layer  # noqa: E402
 from oracle import qi21_oracle as O  # noqa: E402
 from synthetic import device as D  # noqa: E402
 from synthetic import qi21_inputs as S  # noqa: E402
@@ -196,3 +196,31 @@ def test_prefill_cache_rows_are_the_panel_k_v_bits(name):
     panel = dw.ws[off:off + lp * 3 * H * 2].view(torch.int16).view(lp, 3 * H)
     kv = dw.caches[0].layer_tensor(w.layers - 1).view(torch.int16)
     assert torch.equal(kv, panel[:, H:])
+
+
+def test_tiny_block_against_the_unrounded_f32_weights():
+    # for information: the device runs the f16-rounded weights (the bar is
+    # against the oracle on exactly those); the oracle on the unrounded f32
+    # draws shows what the weight rounding itself moves (about 2^-11 / sqrt(3)
+    # of each weight, spread over the block's projections)
+    w = S.WORKLOADS["tiny_block_d256"]
+    run = DeviceRun(w, keep_prefill_x=False)
+    cfg = O.cfg_of(w)
+    W32 = {}
+    for tag in S.WEIGHT_TAGS:
+        r, c = S.weight_shape(w, tag)
+        W32[tag] = S.normal(w.seed, tag, 0, r * c, c ** -0.5).reshape(r, c)
+    W32["norm_q"] = S.norm_weight(w, 0, "norm_q")
+    W32["norm_k"] = S.norm_weight(w, 0, "norm_k")
+    segs = w.segs(0)
+    cache, _ = O.prefill(S.x_prefix(w), [W32], S.mods0(w), segs, cfg)
+    ref32, _ = O.step(S.x_target(w), [W32], S.mods_t(w), segs, cache, cfg)
+    cache16, _ = O.prefill(S.x_prefix(w), [S.layer_weights(w, 0)], S.mods0(w), segs, cfg)
+    ref16, _ = O.step(S.x_target(w), [S.layer_weights(w, 0)], S.mods_t(w), segs, cache16, cfg)
+    got = host(run.out)
+    x0 = S.x_target(w).astype(np.float64)
+    e32 = rel_l2(got, ref32)
+    d32 = rel_l2(got - x0, ref32 - x0)
+    print(f"tiny_block_d256 vs oracle on f32 weights: block rel L2 {e32:.2e}, delta {d32:.2e}; "
+          f"vs f16-rounded weights {rel_l2(got, ref16):.2e}; the two oracles differ by {rel_l2(ref16, ref32):.2e}")
+    assert np.isfinite(e32) and e32 < 2e-3

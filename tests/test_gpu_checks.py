@@ -120,3 +120,60 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     dw.prefill_all()
     dw.step()
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["tiny_block_d256", "tiny_block_d256_bf16"])
+def test_amax_probe_records_the_stored_maxima(name):
+    # QI21_CHECK_AMAX: the largest |value| stored at each 16-bit site of a
+    # pass (the page's AMAX probe). A one-layer step leaves its qkv panel,
+    # attention output, second LayerNorm rows and SwiGLU rows in the
+    # workspace: their maxima equal the recorded ones exactly; the first
+    # LayerNorm's rows are overwritten, so attn-in is checked against the
+    # oracle within one rounding of the 16-bit type.
+    from oracle import qi21_oracle as O
+    from synthetic import device as D
+    w = S.WORKLOADS[name]
+    dw = D.DeviceWorkload(w)
+    q.amax_read(reset=True)
+    prev = q.set_checks(q.CHECK_AMAX)
+    try:
+        dw.prefill_all()
+        pre = q.amax_read(reset=True)
+        _, l0 = q.profile_read()
+        dw.step()
+        got = q.amax_read(reset=True)
+        _, l1 = q.profile_read()
+    finally:
+        q.set_checks(prev)
+    # the prefill of one layer stops after the qkv projection
+    assert pre["attn-in"] > 0 and pre["qkv"] > 0
+    assert pre["attn-out"] == 0 and pre["ffn-in"] == 0 and pre["hidden"] == 0
+    assert l1["misc"] - l0["misc"] == 1 + 5  # the modulation prep and five probes
+    M, H, I = w.n_target, w.dim, w.mlp_hidden
+
+    def a256(v):
+        return (v + 255) // 256 * 256
+
+    xn = a256(M * H * 4)
+    panel = xn + a256(M * H * 2)
+    att = panel + a256(M * 3 * H * 2)
+    hid = att + a256(M * H * 2)
+    dt = q.dtype_of(dw.g)
+
+    def mx(off, count):
+        return float(dw.ws[off:off + count * 2].view(dt).float().abs().max())
+
+    assert got["ffn-in"] == mx(xn, M * H)
+    assert got["qkv"] == mx(panel, M * 3 * H)
+    assert got["attn-out"] == mx(att, M * H)
+    assert got["hidden"] == mx(hid, M * I)
+    ref = float(np.abs(O.norm_mod(S.x_target(w), S.mods_t(w)[:H], w.eps)).max())
+    u = 2.0 ** (-8 if w.dtype == "bf16" else -11)
+    assert abs(got["attn-in"] - ref) <= 2 * u * ref
+    assert all(v == 0 for v in q.amax_read(reset=False).values())
+    # with the flag off nothing is probed
+    _, l2 = q.profile_read()
+    dw.step()
+    _, l3 = q.profile_read()
+    assert l3["misc"] - l2["misc"] == 1
+    assert all(v == 0 for v in q.amax_read(reset=False).values())
