@@ -21,8 +21,12 @@ is stored per layer is small:
   rows, 32 x dim). Their relative L2 difference estimates that of the whole
   output, every row and column included.
 
-The file is keyed by the oracle file's sha256 and by a fingerprint of the
-seeded inputs, so a test can tell a stale file. One workload per run:
+The file is keyed by the sha256 of the oracle functions on the path and by
+a summary of the seeded inputs (per tensor: count, sum and sum of squares),
+so a test can tell a stale file. The summary is compared within a relative
+1e-6, not bit for bit: float32 normal draws can differ in the last place
+between platforms' libm (rare tail samples), which moves no result here.
+One workload per run:
 
     python tests/golden/make_fullwidth_golden.py step32_cond4114_n4096
 
@@ -92,6 +96,52 @@ def inputs_fingerprint(w: S.Workload) -> str:
     return h.hexdigest()
 
 
+def _input_tensors(w: S.Workload):
+    """(name, values) of the draws the chain starts from: every sequence's
+    prefix, the target rows, both modulations and the first and last
+    layers' weights."""
+    for s in range(w.nseq):
+        yield f"x_prefix_{s}", S.x_prefix(w, s)
+    yield "x_target", S.x_target(w)
+    yield "mods_t", S.mods_t(w)
+    yield "mods0", S.mods0(w)
+    for layer in sorted({0, w.layers - 1}):
+        W = S.layer_weights(w, layer)
+        for tag in S.WEIGHT_TAGS + ("norm_q", "norm_k"):
+            yield f"{tag}_{layer}", W[tag]
+
+
+def inputs_summary(w: S.Workload) -> list:
+    """[name, count, sum, sum of squares] (float64) of each input tensor."""
+    out = []
+    for name, a in _input_tensors(w):
+        v = np.asarray(a, dtype=np.float64).ravel()
+        out.append([name, int(v.size), float(v.sum()), float((v * v).sum())])
+    return out
+
+
+def summary_matches(stored, now, rtol=1e-6) -> bool:
+    """Same tensors, counts, and sums within rtol of the tensor's L2 scale."""
+    if len(stored) != len(now):
+        return False
+    for (n0, c0, s0, q0), (n1, c1, s1, q1) in zip(stored, now):
+        scale = max(np.sqrt(q0), 1e-30)
+        if n0 != n1 or c0 != c1 or abs(s0 - s1) > rtol * scale or abs(q0 - q1) > rtol * max(q0, 1e-30):
+            return False
+    return True
+
+
+def stale_reason(meta, name: str):
+    """Why a stored file cannot be used for workload `name` (None: usable)."""
+    if meta is None:
+        return f"tests/golden/fullwidth_{name}.npz has not been written"
+    if meta.get("oracle_sha256") != oracle_sha256():
+        return f"fullwidth_{name}.npz was written by another oracle version"
+    if "inputs_summary" not in meta or not summary_matches(meta["inputs_summary"], inputs_summary(S.WORKLOADS[name])):
+        return f"fullwidth_{name}.npz was written for other seeded inputs"
+    return None
+
+
 def sketch_of(X: np.ndarray, A: np.ndarray, B: np.ndarray) -> np.ndarray:
     """A X B^T in float64 (the parity statistic; not part of the method)."""
     return (A @ np.asarray(X, dtype=np.float64)) @ B.T
@@ -148,6 +198,7 @@ def run(name: str, out_dir: str = HERE) -> str:
         "format": FORMAT,
         "oracle_sha256": oracle_sha256(),
         "inputs_fingerprint": inputs_fingerprint(w),
+        "inputs_summary": inputs_summary(w),
         "sketch_k": SKETCH_K,
         "seed": w.seed,
         "nseq": w.nseq,
@@ -173,6 +224,26 @@ def load(name: str, golden_dir: str = HERE):
     return meta, arrays
 
 
+def refresh_meta(name: str, golden_dir: str = HERE) -> None:
+    """Rewrite only the keys of a stored file (the oracle source hash and
+    the input summary, recomputed here); its arrays are kept as written."""
+    path = os.path.join(golden_dir, f"fullwidth_{name}.npz")
+    z = np.load(path)
+    arrays = {k: z[k] for k in z.files if k != "meta"}
+    meta = json.loads(bytes(z["meta"]).decode())
+    w = S.WORKLOADS[name]
+    if meta["inputs_fingerprint"] != inputs_fingerprint(w):
+        raise SystemExit(f"{name}: the inputs here are not the ones the file was written for")
+    meta["inputs_summary"] = inputs_summary(w)
+    arrays["meta"] = np.frombuffer(json.dumps(meta).encode(), dtype=np.uint8)
+    np.savez_compressed(path, **arrays)
+    print(f"refreshed the keys of {path}")
+
+
 if __name__ == "__main__":
-    for nm in sys.argv[1:]:
-        run(nm)
+    if len(sys.argv) > 2 and sys.argv[1] == "--refresh-meta":
+        for nm in sys.argv[2:]:
+            refresh_meta(nm)
+    else:
+        for nm in sys.argv[1:]:
+            run(nm)

@@ -3,6 +3,7 @@
 from oracle/ and synthetic/ only) are current and come from the oracle: their
 keys match the present oracle source and seeded inputs, and a piece of one
 of them is recomputed here from the oracle directly. No GPU."""
+import dataclasses
 import os
 import sys
 
@@ -27,7 +28,7 @@ def test_stored_file_is_current(name):
     w = S.WORKLOADS[name]
     assert meta["workload"] == name and meta["layers"] == w.layers and meta["nseq"] == w.nseq
     assert meta["oracle_sha256"] == G.oracle_sha256(), "the oracle changed: rewrite the stored file"
-    assert meta["inputs_fingerprint"] == G.inputs_fingerprint(w), "the seeded inputs changed"
+    assert G.stale_reason(meta, name) is None
     L, K = w.layers, meta["sketch_k"]
     np.testing.assert_array_equal(arr["rows"], G.sample_rows(w.n_target))
     for s in range(w.nseq):
@@ -62,6 +63,20 @@ def test_first_layer_of_the_cfg_pair_recomputed_from_the_oracle():
     k_sk = G.sketch_of(cache[0][0], Ap, B)
     want_k = arr[f"k_sketch_s{s}"][0].astype(np.float64)
     assert np.max(np.abs(k_sk - want_k)) <= 1e-5 * np.max(np.abs(want_k))
+
+
+def test_input_summary_tolerates_last_place_noise_only():
+    w = S.WORKLOADS["cfg_pair_d256"]
+    now = G.inputs_summary(w)
+    assert G.summary_matches(now, now)
+    # a last-place change of a few elements is tolerated
+    noisy = [[n, c, s_ * (1 + 1e-9), q_ * (1 + 1e-9)] for n, c, s_, q_ in now]
+    assert G.summary_matches(now, noisy)
+    # another seed is not
+    other = G.inputs_summary(dataclasses.replace(w, seed=1))
+    assert not G.summary_matches(now, other)
+    shifted = [[n, c, s_ + 1e-3 * np.sqrt(q_), q_] for n, c, s_, q_ in now]
+    assert not G.summary_matches(now, shifted)
 
 
 def test_sketch_estimates_the_whole_relative_error():

@@ -10,7 +10,7 @@ per layer a few target rows element by element, and Gaussian sketches
 A X B^T of the step output, of the prefill output and of the cached K and V
 (32 x 32 numbers that weigh every row and column; their relative L2
 difference estimates that of the whole tensor). A stored file whose oracle
-source hash or input fingerprint no longer matches is skipped with the
+source hash or input summary no longer matches is skipped with the
 reason, never trusted.
 
 Bar: rel L2 <= 2e-3 for every block output (step and prefill) and for the
@@ -40,12 +40,9 @@ KV_TOL = 2e-3
 
 def _golden(name):
     meta, arr = G.load(name)
-    if meta is None:
-        pytest.skip(f"tests/golden/fullwidth_{name}.npz has not been written")
-    if meta["oracle_sha256"] != G.oracle_sha256():
-        pytest.skip(f"fullwidth_{name}.npz was written by another oracle version")
-    if meta["inputs_fingerprint"] != G.inputs_fingerprint(S.WORKLOADS[name]):
-        pytest.skip(f"fullwidth_{name}.npz was written for other seeded inputs")
+    why = G.stale_reason(meta, name)
+    if why is not None:
+        pytest.skip(why)
     return meta, arr
 
 
