@@ -21,7 +21,7 @@ __all__ = [
     "workspace_bytes", "pack_layer", "prefill", "step", "step_noalloc", "step_batch", "embed", "final",
     "timestep_mods", "denoise", "set_checks", "PackedLayerFp8", "pack_layer_fp8", "workspace_bytes_fp8",
     "prefill_fp8", "step_batch_fp8", "op_quant_rows", "op_rowop_fp8", "op_gemm_fp8", "Graph", "graph_step_batch", "graph_step_batch_fp8", "graph_denoise_batch", "count_nonfinite", "CHECK_FINITE", "CHECK_AMAX", "AMAX_SITES", "amax_read", "denoise_batch", "device_status", "selftest_wait_timeout", "build",
-    "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_qkrope", "op_kvcopy", "op_attention",
+    "profile_enable", "profile_read", "CLASSES", "op_rowop", "op_mods_prep", "op_gemm", "op_gemm_split", "op_qkrope", "op_kvcopy", "op_attention",
 ]
 
 
@@ -453,6 +453,21 @@ def op_gemm(epi, A, Bw, out, gate_t=None, stream=None):
     check(load().qi21_op_gemm(_dt_code(A), epi, M, N, K, _ptr(A, None, "A"), _ptr(Bw, A.dtype, "B"),
                               _ptr(out, None, "out"), out.shape[1], _ptr(gate_t, torch.float32, "gate_t"),
                               _stream(stream)))
+
+
+def op_gemm_split(epi, A, Bw, out, scratch, gate_t=None, stream=None):
+    """qi21_op_gemm_split: qi21_op_gemm with the K-split tail, merged
+    through `scratch` (a 256-byte aligned device buffer); returns the part
+    count used (1: no split)."""
+    torch = _torch()
+    M, K = A.shape
+    N = Bw.shape[0]
+    parts = C.c_int32(0)
+    check(load().qi21_op_gemm_split(_dt_code(A), epi, M, N, K, _ptr(A, None, "A"), _ptr(Bw, A.dtype, "B"),
+                                    _ptr(out, None, "out"), out.shape[1], _ptr(gate_t, torch.float32, "gate_t"),
+                                    _ptr(scratch, None, "scratch"), scratch.numel() * scratch.element_size(),
+                                    C.byref(parts), _stream(stream)))
+    return parts.value
 
 
 def op_qkrope(panel, heads, norm_q, norm_k, cos_, sin_, eps=1e-6, stream=None):

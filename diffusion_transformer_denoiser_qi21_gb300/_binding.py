@@ -112,6 +112,8 @@ _SIGS = {
     "qi21_op_rowop": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_op_mods_prep": (C.c_int, [_i32, _vp, _vp, _vp]),
     "qi21_op_gemm": (C.c_int, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "qi21_op_gemm_split": (C.c_int, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _sz,
+                                     C.POINTER(_i32), _vp]),
     "qi21_op_qkrope": (C.c_int, [_i32, _i32, _i32, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qi21_op_kvcopy": (C.c_int, [_i32, _i32, _vp, _vp, _vp]),
     "qi21_op_attention": (C.c_int, [_i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),

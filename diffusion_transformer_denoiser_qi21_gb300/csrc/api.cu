@@ -261,7 +261,7 @@ static int elem_of(const qi21_geom* g) { return g->dtype == QI21_DTYPE_BF16 ? QI
 static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t x, xn, panel, att, hid, md, q8, qs, total;
+  size_t x, xn, panel, att, hid, md, flags, q8, qs, total;
 };
 
 // fp8: the E4M3 activation rows (one buffer [M][max(H, I)] shared by xn,
@@ -282,6 +282,9 @@ static WsLayout ws_layout(const qi21_geom* g, int rows, bool fp8 = false) {
   off = align256(off + M * I * 2);
   w.md = off;
   off = align256(off + 4 * H * 4);
+  // merge flags of the GEMMs' K-split tails (zeroed at the start of a pass)
+  w.flags = off;
+  off = align256(off + kGemmFlagBytes);
   w.q8 = w.qs = 0;
   if (fp8) {
     w.q8 = off;
@@ -640,6 +643,7 @@ struct PassBufs {
   void* att;    // dt [M][H]
   void* hid;    // dt [M][I]
   float* md;
+  int* flags;   // K-split tail merge flags (kGemmFlagBytes)
   uint8_t* q8;  // FP8 pass: E4M3 activation rows (xn, att, hid in turn)
   float* qs;    // FP8 pass: their row scales
 };
@@ -652,6 +656,13 @@ struct LayerPlan {
   bool has_attn;  // false for the prefill's last layer (stops after its cache write)
 };
 
+static void split_scratch(GemmPlan* p, void* part, size_t bytes, int* flags, int epoch) {
+  p->part = part;
+  p->part_bytes = bytes;
+  p->flags = flags;
+  p->epoch = epoch;
+}
+
 // Plans of every layer of a pass, encoded before the pass enqueues anything
 // (so an encoding failure at any layer leaves the stream untouched). Exactly
 // one of layers (16-bit planes) and l8 (the FP8 variant: E4M3 planes, every
@@ -663,6 +674,9 @@ int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8
   const int H = g->dim, I = g->mlp_hidden, L = g->layers, dt = g->dtype;
   const float* g1 = b.md + H;
   const float* g2 = b.md + 3 * H;
+  // 16-bit hid / panel bytes; the FP8 pass keeps its 16-bit buffers too
+  const size_t hid_bytes = static_cast<size_t>(M) * I * 2;
+  const size_t panel_bytes = static_cast<size_t>(M) * 3 * H * 2;
   RopeTables tabs{};
   if (prefill) {
     tabs.nsrc = 1;
@@ -690,6 +704,7 @@ int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8
     lp.kv = prefill ? static_cast<uint16_t*>(pcache->kv) + static_cast<size_t>(l) * pcache->lp * 2 * H : nullptr;
     // a prefill's K|V cache rows are written by the qkv epilogue itself
     lp.pq.qkv = QkvEpi{norm_q, norm_k, g->eps, H, tabs, lp.kv};
+    split_scratch(&lp.pq, b.hid, hid_bytes, b.flags, 4 * l + 1);
     lp.has_attn = !(prefill && last);
     if (!lp.has_attn) break;
     AttnArgs aa{};
@@ -723,6 +738,11 @@ int plan_pass(const qi21_geom* g, const qi21_layer* layers, const qi21_layer_fp8
               "w13 plan");
       QI21_CK(make_gemm_plan(&lp.p2, EPI_RESID, dt, M, H, I, b.hid, layers[l].w2, b.x, H, g2), "down plan");
     }
+    // K-split tails: the partials go to a buffer the GEMM neither reads nor
+    // writes (hid during qkv and o, the panel during gate/up and down)
+    split_scratch(&lp.po, b.hid, hid_bytes, b.flags, 4 * l + 2);
+    split_scratch(&lp.p13, b.panel, panel_bytes, b.flags, 4 * l + 3);
+    split_scratch(&lp.p2, b.panel, panel_bytes, b.flags, 4 * l + 4);
   }
   return QI21_OK;
 }
@@ -774,6 +794,9 @@ int exec_pass(const qi21_geom* g, bool f8, int M, bool prefill, const PassBufs& 
     return QI21_OK;
   };
   int rc;
+  // the K-split tails' merge flags start at zero; each GEMM of the pass
+  // sets them to its own epoch
+  QI21_CK(cudaMemsetAsync(b.flags, 0, kGemmFlagBytes, s), "flags reset");
   if ((rc = ln(s1)) != QI21_OK) return rc;
   for (int l = 0; l < L; ++l) {
     const LayerRange range(prefill, l);
@@ -831,6 +854,7 @@ int ws_bind(const qi21_geom* g, int M, void* ws, size_t ws_bytes, PassBufs* b, b
   b->att = base + w.att;
   b->hid = base + w.hid;
   b->md = reinterpret_cast<float*>(base + w.md);
+  b->flags = reinterpret_cast<int*>(base + w.flags);
   b->q8 = fp8 ? base + w.q8 : nullptr;
   b->qs = fp8 ? reinterpret_cast<float*>(base + w.qs) : nullptr;
   return QI21_OK;
@@ -1247,6 +1271,34 @@ int qi21_op_gemm(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, co
   GemmPlan p;
   QI21_CK(make_gemm_plan(&p, epi, dtype, M, N, K, A, B, out, ldo, gate_t), "gemm plan");
   QI21_CK(launch_gemm(p, static_cast<cudaStream_t>(stream)), "gemm");
+  return QI21_OK;
+}
+
+int qi21_op_gemm_split(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, const void* A, const void* B,
+                       void* out, int32_t ldo, const float* gate_t, void* scratch, size_t scratch_bytes,
+                       int32_t* parts_out, void* stream) {
+  if (parts_out) *parts_out = 1;
+  if (dtype_check(dtype) != QI21_OK) return QI21_ERR_ARG;
+  if (epi < 0 || epi > 3) return fail(QI21_ERR_ARG, "epilogue %d", epi);
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 64) return fail(QI21_ERR_SHAPE, "M %d N %d K %d", M, N, K);
+  if (M == 0) return QI21_OK;
+  if (!A || !B || !out || (epi == EPI_RESID && !gate_t)) return fail(QI21_ERR_ARG, "null pointer");
+  if (!scratch || scratch_bytes < kGemmFlagBytes) return fail(QI21_ERR_WORKSPACE, "scratch below %zu bytes", kGemmFlagBytes);
+  if (reinterpret_cast<uintptr_t>(scratch) % 256) return fail(QI21_ERR_WORKSPACE, "scratch must be 256-byte aligned");
+  const int cols = epi == EPI_SWIGLU ? N / 2 : N;
+  if (ldo < cols || ldo % 8) return fail(QI21_ERR_SHAPE, "ldo %d", ldo);
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(QI21_ERR_ARG, "A, B and out must be 16-byte aligned");
+  GemmPlan p;
+  QI21_CK(make_gemm_plan(&p, epi, dtype, M, N, K, A, B, out, ldo, gate_t), "gemm plan");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int parts = 1;
+  split_scratch(&p, static_cast<uint8_t*>(scratch) + kGemmFlagBytes, scratch_bytes - kGemmFlagBytes,
+                static_cast<int*>(scratch), 1);
+  p.parts_out = &parts;
+  QI21_CK(cudaMemsetAsync(scratch, 0, kGemmFlagBytes, s), "flags reset");
+  QI21_CK(launch_gemm(p, s), "gemm");
+  if (parts_out) *parts_out = parts;
   return QI21_OK;
 }
 

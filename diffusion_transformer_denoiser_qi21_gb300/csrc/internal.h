@@ -116,7 +116,6 @@ struct QkvEpi {
 struct GemmPlan {
   CUtensorMap tmA;  // A dt [M][K], box 64 x 128, 128B swizzle
   CUtensorMap tmB;  // B dt [N][K], box 64 x BN, 128B swizzle
-  CUtensorMap tmBh; // B dt [N][K], box 64 x BN/2 (split tiles of a partial last wave)
   CUtensorMap tmX;  // EPI_RESID: x f32 [M][ldo], box 32 x 32, 128B swizzle
   int M, N, K, bn, epi, ldo;
   int dt;            // operand and 16-bit output type (f16 path); DT_F16 for FP8
@@ -126,7 +125,23 @@ struct GemmPlan {
   bool f8;           // E4M3 operands (tensor maps of bytes, box 128 x rows)
   const float* sa;   // FP8: per A row scale
   const float* sw;   // FP8: per B row scale
+  // K-split tail (optional, set after make_gemm_plan*): scratch for the
+  // partials of a partial last wave and the merge flags, which a launch sets
+  // to `epoch` (>= 1; zero them before the first launch and give each launch
+  // between two zeroings its own epoch)
+  void* part;
+  size_t part_bytes;
+  int* flags;
+  int epoch;
+  int* parts_out;  // optional (host): the part count a launch used (1: no split)
 };
+
+// K-split tail limits: parts per tail tile, flag bytes (ints: tail tiles x
+// parts x 8), and the partial bytes of `tail_tiles` tiles split in `parts`
+// (one BN x 32 f32 slab per tile, part, CTA and epilogue warp).
+constexpr int kMaxKParts = 8;
+constexpr size_t kGemmFlagBytes = 4096;
+size_t gemm_split_bytes(int bn, int tail_tiles, int parts);
 
 // Encode the tensor maps of C = A B^T with A, B of type dt. Returns
 // cudaSuccess or an error; launches nothing.

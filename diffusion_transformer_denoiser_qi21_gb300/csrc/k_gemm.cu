@@ -89,7 +89,14 @@ struct GemmCfg {
   static constexpr int kStages = (192 * 1024) / kStageBytes;
   static constexpr int kEpiOff = kStages * kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kBarBytes = 256;
+  // a cluster's last work item: each epilogue warp may use 48 KB of the
+  // (then idle) operand ring for its x chunks and the other K-split parts'
+  // partials, and 8 single-use barriers for those x chunks
+  static constexpr int kTailWarpBytes = 48 * 1024;
+  static_assert(4 * kTailWarpBytes <= kStages * kStageBytes, "tail staging exceeds the operand ring");
+  static_assert(BN * 128 <= kTailWarpBytes, "tail staging of one warp");
+  static constexpr int kBarBytes = 512;
+  static_assert((2 * kStages + 4 + 4 * kXBufs + 32) * 8 + 8 <= kBarBytes, "barrier region");
   static constexpr int kSmem = kEpiOff + kEpiBytes + kBarBytes + 1024;
 };
 
@@ -100,6 +107,73 @@ struct EpiArgs {
   QkvEpi qkv;
   const float* sa;  // FP8: per A row
   const float* sw;  // FP8: per B row (output column)
+  // K-split tail: raw f32 partials, one slab per (tail tile, part, CTA
+  // rank, epilogue warp) of [BN columns][32 rows] (a part writes the
+  // columns it does not own), and one ready flag per slab, set to `epoch`
+  float* part;
+  int* flags;
+  int parts;
+  int epoch;
+};
+
+// Bounded wait (acquire) for *f == want, by one thread; false if it gave up.
+__device__ __forceinline__ bool wait_flag(const int* f, int want, volatile int* abort, unsigned int* status) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v == want) return true;
+    if (*abort) return false;
+    __nanosleep(32);
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void set_flag_release(int* f, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+// 16-byte global -> shared copy (cp.async, L2 only), its group commit and
+// the wait for all of this thread's groups.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// A split tail tile's owner of columns [o0, o0 + w) sums, per element of
+// this thread's row, every part's value in part order (its own accumulator
+// at its own place, the others' staged partials), so the result does not
+// depend on which part owns the columns.
+struct PartSum {
+  const float* st;  // this warp's staged partials [other part][w][32], null if none
+  int parts, own, w, o0;
+  // kTwo: the caller never splits in more than two parts (128-column owners
+  // of a 256-column tile)
+  template <bool kTwo = false>
+  __device__ __forceinline__ void add(uint32_t (&r)[32], int col) const {
+    if (st == nullptr) return;
+    const float* b = st + static_cast<size_t>(col - o0) * 32 + (threadIdx.x & 31);
+    if (kTwo || parts == 2) {  // one other part; a + b == b + a, whichever part owns
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + b[e * 32]);
+      return;
+    }
+    const size_t slot = static_cast<size_t>(w) * 32;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float a = __uint_as_float(r[e]);
+      float s = own == 0 ? a : b[e * 32];
+      for (int pp = 1; pp < parts; ++pp) s += pp == own ? a : b[(pp < own ? pp : pp - 1) * slot + e * 32];
+      r[e] = __float_as_uint(s);
+    }
+  }
+  __device__ __forceinline__ void operator()(uint32_t (&r)[32], int col) const { add<false>(r, col); }
 };
 
 // FP8: 32 accumulator columns starting at column `col` times sa sw[col + i]
@@ -118,11 +192,14 @@ __device__ __forceinline__ void f8_scale(uint32_t (&r)[32], float sa, const floa
   }
 }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
+// silu(v) = v / (1 + e^-v) with the approximate exponential and divide
+// (relative error ~2^-21, far below the 16-bit rounding of the output)
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
 
+// Epilogue of one row over accumulator columns [o0, o1) of the tile.
 template <int BN, int EPI, int OP>
-__device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0, int bn,
-                                              const EpiArgs& ep) {
+__device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, int n0, int o0, int o1,
+                                              const EpiArgs& ep, const PartSum& padd) {
   constexpr bool F8 = OP == kOpF8;
   constexpr bool BF = OP == kOpBF16;  // 16-bit outputs in bf16
   const bool live = row < M;
@@ -130,7 +207,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
   if constexpr (EPI == EPI_SWIGLU) {
     uint16_t* out = static_cast<uint16_t*>(ep.out) + static_cast<size_t>(row) * ep.ldo + n0 / 2;
 #pragma unroll 1
-    for (int p = 0; p < bn / 128; ++p) {
+    for (int p = o0 / 128; p < o1 / 128; ++p) {
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t g[32], u[32];
@@ -138,6 +215,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
         tmem_ld32(tbase + p * 128 + 64 + c * 32, u);
         tmem_ld_wait(g);
         tmem_ld_wait(u);
+        padd.add<true>(g, p * 128 + c * 32);
+        padd.add<true>(u, p * 128 + 64 + c * 32);
         f8_scale<OP>(g, sa, ep.sw, n0 + p * 128 + c * 32);
         f8_scale<OP>(u, sa, ep.sw, n0 + p * 128 + 64 + c * 32);
         if (live) {
@@ -169,7 +248,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     const float4* cs4 = reinterpret_cast<const float4*>(qe.tabs.src[si].cos_ + trow);
     const float4* sn4 = reinterpret_cast<const float4*>(qe.tabs.src[si].sin_ + trow);
 #pragma unroll 1
-    for (int hc = 0; hc < bn / 128; ++hc) {
+    for (int hc = o0 / 128; hc < o1 / 128; ++hc) {
       const int col = n0 + hc * 128;
       const int part = col / qe.H;  // 0 q, 1 k, 2 v (uniform over the tile)
       uint32_t r[4][32];
@@ -177,6 +256,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
       for (int c = 0; c < 4; ++c) tmem_ld32(tbase + hc * 128 + c * 32, r[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) padd.add<true>(r[c], hc * 128 + c * 32);
       if (!live) continue;
 #pragma unroll
       for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
@@ -240,10 +321,11 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     }
   } else {
 #pragma unroll 1
-    for (int c = 0; c < bn / 32; ++c) {
+    for (int c = o0 / 32; c < o1 / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tbase + c * 32, r);
       tmem_ld_wait(r);
+      padd(r, c * 32);
       if (!live) continue;
       const int col = n0 + c * 32;
       f8_scale<OP>(r, sa, ep.sw, col);
@@ -283,11 +365,14 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
   }
 }
 
-// Tile pair t of the persistent schedule (one pair per cluster step): the
-// first nfull pairs are 2 x (BM x BN) with pair row mp (tile rows 2 mp and
-// 2 mp + 1) and column block nb; when the last wave would be at most half
-// full, its pairs are split into two halves of BN/2 columns (same K order
-// per output element, so identical results) that fill one half-length wave.
+// Work item t of the persistent schedule (one per cluster step): the first
+// nfull items are whole 2 x (BM x BN) tiles with pair row mp (tile rows
+// 2 mp and 2 mp + 1) and column block nb; when the last wave is partial,
+// each of its tiles is split along K into `parts` items of k-blocks
+// [part nk / parts, (part + 1) nk / parts) that run side by side in one
+// shorter wave (whole tiles, so every SM streams operands at the rate of a
+// full tile); parts 0 .. parts-2 store raw partials, the last part adds
+// them in order and runs the epilogue.
 // Full tile f lies in group f / (G nN) of G pair rows (the last group may
 // be smaller); inside a group the pair rows run fastest, then the column
 // blocks, so the clusters of a wave work on a band of about G pair rows and
@@ -295,6 +380,9 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 // column blocks. G = num_mp is plain pair-rows-fastest order.
 struct TileInfo {
   int mp, n0, bn;
+  int kb0, kb1;  // k-blocks of this item
+  int part;      // -1 whole tile, else the part of a split tail tile
+  int tail;      // index of the tail tile (split tiles only)
 };
 
 __device__ __forceinline__ void raster(int f, int num_mp, int nN, int G, int& mp, int& nb) {
@@ -308,22 +396,24 @@ __device__ __forceinline__ void raster(int f, int num_mp, int nN, int G, int& mp
 }
 
 template <int BN>
-__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, int nfull) {
+__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, int nfull, int parts, int nk) {
   int mp, nb;
   if (t < nfull) {
     raster(t, num_mp, nN, G, mp, nb);
-    return TileInfo{mp, nb * BN, BN};
+    return TileInfo{mp, nb * BN, BN, 0, nk, -1, 0};
   }
   const int u = t - nfull;
-  raster(nfull + (u >> 1), num_mp, nN, G, mp, nb);
-  return TileInfo{mp, nb * BN + (u & 1) * (BN / 2), BN / 2};
+  const int tail = u / parts;
+  const int part = u - tail * parts;
+  raster(nfull + tail, num_mp, nN, G, mp, nb);
+  return TileInfo{mp, nb * BN, BN, part * nk / parts, (part + 1) * nk / parts, part, tail};
 }
 
 template <int BN, int EPI, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmX, int M,
-                   int N, int K, int group, int nfull, int num_tiles, EpiArgs ep) {
+                   const __grid_constant__ CUtensorMap tmX, int M, int N, int K, int group, int nfull, int num_tiles,
+                   EpiArgs ep) {
   using C = GemmCfg<BN, EPI>;
   constexpr bool F8 = OP == kOpF8;
   extern __shared__ uint8_t smem_raw[];
@@ -334,7 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* xbar = tempty + 2;  // [4][kXBufs] EPI_RESID: x chunk landed, per warp and buffer
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4 * C::kXBufs);
+  // then 4 x 8 single-use barriers of the last item's x chunks
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 4 * C::kXBufs + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -357,14 +448,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 8);  // 4 epilogue warps x 2 CTAs
     }
-    for (int i = 0; i < 4 * C::kXBufs; ++i) mbar_init(&xbar[i], 1);
+    for (int i = 0; i < 4 * C::kXBufs + 32; ++i) mbar_init(&xbar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (nfull < num_tiles) tma_prefetch_desc(&tmBh);
     if (EPI == EPI_RESID) tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
@@ -382,13 +472,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull);
-        const bool half = ti.bn != BN;
+        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
         const int m0 = (2 * ti.mp + rank) * kBM;
-        const int bh = ti.bn / 2;  // B rows this CTA holds
+        const int bh = BN / 2;  // B rows this CTA holds
         // the even CTA's barrier counts both CTAs' A and B bytes
-        const uint32_t bytes = 2u * (C::kABytes + static_cast<uint32_t>(bh) * kBK * 2);
-        for (int kb = 0; kb < nk; ++kb) {
+        const uint32_t bytes = 2u * (C::kABytes + C::kBBytes);
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, &s_gemm_status)) {
             ok = false;
             break;
@@ -397,7 +486,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t fb = mapa_rank(&full[s], 0);
           if (leader) mbar_arrive_expect_tx(&full[s], bytes);
           tma_load_2d_pair(sa, &tmA, fb, kb * kKE, m0);
-          tma_load_2d_pair(sa + C::kABytes, half ? &tmBh : &tmB, fb, kb * kKE, ti.n0 + rank * bh);
+          tma_load_2d_pair(sa + C::kABytes, &tmB, fb, kb * kKE, ti.n0 + rank * bh);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -407,20 +496,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc_full = idesc_f16(2 * kBM, BN, false, OP == kOpBF16);
-      constexpr uint32_t idesc_half = idesc_f16(2 * kBM, BN / 2, false, OP == kOpBF16);
+      constexpr uint32_t idesc = idesc_f16(2 * kBM, BN, false, OP == kOpBF16);
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
       for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
-        const uint32_t idesc = t < nfull ? idesc_full : idesc_half;
+        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, &s_gemm_status)) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, &s_gemm_status)) {
             ok = false;
             break;
@@ -431,10 +519,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of each 128-byte row
+            const uint32_t accumulate = (kb != ti.kb0 || k != 0) ? 1u : 0u;
             if constexpr (F8)
-              tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, accumulate);
             else
-              tc_mma_f16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_f16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, accumulate);
           }
           tc_commit_pair(&empty[s], 0x3);
           if (++s == C::kStages) {
@@ -448,79 +537,164 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int it = 0;
-    int xu = 0;  // EPI_RESID: x chunks this warp has used (buffer xu & 1)
+    int xu = 0;  // EPI_RESID: x chunks this warp has staged in its epilogue buffers
     bool eok = true;
+    // a cluster's last item: this warp's share of the idle operand ring and
+    // its single-use x chunk barriers
+    uint8_t* const wst = smem + q * C::kTailWarpBytes;
+    uint64_t* const xl = xbar + 4 * C::kXBufs + 8 * q;
     for (int t = cluster; t < num_tiles && eok; t += nclusters, ++it) {
-      const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull);
+      const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
+      const bool last = t + nclusters >= num_tiles;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, &s_gemm_status)) break;
       tc_fence_after();
+      // every MMA of this CTA has read its operands: in the last item the
+      // ring may take generic and TMA writes
+      if (last) fence_proxy_async_smem();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      // accumulator columns whose outputs this item writes: all of them, or
+      // for part p of a K-split tail tile (always a cluster's last item)
+      // columns [p w, (p + 1) w)
+      const int P = ti.part >= 0 ? ep.parts : 1;
+      const int w = ti.bn / P;
+      const int o0 = ti.part >= 0 ? ti.part * w : 0, o1 = o0 + w;
+      // the last item's x chunks (EPI_RESID) sit after the staged partials
+      const int xoff = (P - 1) * w * 128;
+      const int row0 = (2 * ti.mp + rank) * kBM + q * 32;  // this warp's first row
+      if (EPI == EPI_RESID && last && lane == 0)
+        for (int c = o0 / 32; c < o1 / 32; ++c) {
+          mbar_arrive_expect_tx(&xl[c - o0 / 32], 4096);
+          tma_load_2d(wst + xoff + (c - o0 / 32) * 4096, &tmX, &xl[c - o0 / 32], ti.n0 + 32 * c, row0);
+        }
+      PartSum psum{nullptr, 1, 0, 0, 0};
+      if (ti.part >= 0) {
+        // hand the other columns to their owners through this part's slab,
+        // then sum the other parts' slices of the own columns (staged in
+        // the ring) with the accumulator
+        const size_t slab = static_cast<size_t>(BN) * 32;
+        const size_t sbase = static_cast<size_t>(ti.tail) * P * 8 + rank * 4 + q;  // + 8 per part
+        float* mine = ep.part + (sbase + ti.part * 8) * slab + lane;
+#pragma unroll 1
+        for (int c = 0; c < ti.bn / 32; ++c) {
+          if (c * 32 >= o0 && c * 32 < o1) continue;
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) __stcg(mine + static_cast<size_t>(c * 32 + e) * 32, __uint_as_float(r[e]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) set_flag_release(ep.flags + sbase + ti.part * 8, ep.epoch);
+        bool got = last;  // the schedule guarantees it; anything else is refused, not raced
+        if (!last && lane == 0) {
+          *abort_flag = 1;
+          atomicOr(&s_gemm_status, kStatusTimeout);
+        }
+        if (lane == 0)
+          for (int pp = 0; pp < P && got; ++pp)
+            if (pp != ti.part) got = wait_flag(ep.flags + sbase + pp * 8, ep.epoch, abort_flag, &s_gemm_status);
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          // let the x loads issued above land before the CTA leaves
+          if (EPI == EPI_RESID && last && lane == 0)
+            for (int c = o0 / 32; c < o1 / 32; ++c) mbar_wait_drain(&xl[c - o0 / 32], 0);
+          __syncwarp();
+          eok = false;
+          break;
+        }
+        __threadfence();
+        float* st = reinterpret_cast<float*>(wst);
+        int slot = 0;
+        for (int pp = 0; pp < P; ++pp) {
+          if (pp == ti.part) continue;
+          const float* src = ep.part + (sbase + pp * 8) * slab + static_cast<size_t>(o0) * 32;
+          float* dst = st + static_cast<size_t>(slot) * w * 32;
+          for (int i = lane; i < w * 8; i += 32) cp_async16(dst + 4 * i, src + 4 * i);
+          ++slot;
+        }
+        cp_async_commit_wait_all();
+        __syncwarp();
+        psum = PartSum{st, P, ti.part, w, o0};
+      }
       if constexpr (EPI == EPI_RESID) {
         // x += tanh(g) acc for this warp's 32 rows, 32 columns at a time:
-        // TMA loads the x chunk (128-byte swizzled rows) into one of two
-        // buffers, each thread updates its row there, TMA stores it back
+        // TMA loads the x chunk (128-byte swizzled rows) into shared memory,
+        // each thread updates its row there, TMA stores it back. Earlier
+        // items cycle through kXBufs buffers, kXBufs - 1 loads ahead (their
+        // epilogue hides behind the next item's MMAs); the last item, whose
+        // epilogue nothing hides, has every chunk's load in flight at once
+        // in the idle ring.
         constexpr int NB = C::kXBufs;
         uint8_t* eb = smem + C::kEpiOff + q * NB * 4096;
         uint64_t* xb = xbar + NB * q;
-        const int row0 = (2 * ti.mp + rank) * kBM + q * 32;
         const int row = row0 + lane;
         const float sa = (F8 && row < M) ? ep.sa[row] : 1.f;
-        const int nch = ti.bn / 32;
-        int issued = 0;  // x chunks of this tile whose loads were issued
+        const int c0 = o0 / 32, c1 = o1 / 32;
+        int issued = last ? c1 : c0;  // x chunks of this item whose loads were issued (a last item's: above)
+        auto buf = [&](int c) -> uint8_t* { return last ? wst + xoff + (c - c0) * 4096 : eb + ((xu + c - c0) % NB) * 4096; };
+        auto bar = [&](int c) -> uint64_t* { return last ? &xl[c - c0] : &xb[(xu + c - c0) % NB]; };
+        auto par = [&](int c) -> uint32_t { return last ? 0u : static_cast<uint32_t>((xu + c - c0) / NB) & 1u; };
         auto load = [&](int c) {
           if (lane == 0) {
-            const int b = (xu + c) % NB;
-            bulk_wait_read_all();  // the store that used buffer b last has read it
-            mbar_arrive_expect_tx(&xb[b], 4096);
-            tma_load_2d(eb + b * 4096, &tmX, &xb[b], ti.n0 + 32 * c, row0);
+            if (!last) bulk_wait_read_all();  // the store that used this buffer last has read it
+            mbar_arrive_expect_tx(bar(c), 4096);
+            tma_load_2d(buf(c), &tmX, bar(c), ti.n0 + 32 * c, row0);
           }
           issued = c + 1;
         };
-        for (int c = 0; c < NB - 1 && c < nch; ++c) load(c);
-        for (int c = 0; c < nch; ++c) {
-          if (c + NB - 1 < nch && !*abort_flag) load(c + NB - 1);
+        const int ahead = last ? c1 - c0 : NB - 1;
+        if (!last)
+          for (int c = c0; c < c0 + ahead && c < c1; ++c) load(c);
+        for (int c = c0; c < c1; ++c) {
+          if (c + ahead < c1 && !*abort_flag) load(c + ahead);
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
-          const int u = xu + c;
-          const bool got =
-              mbar_wait(&xb[u % NB], static_cast<uint32_t>(u / NB) & 1u, abort_flag, &s_gemm_status);
+          // the gate values while the x chunk lands
+          float4 gv[8];
+          const float4* g4 = reinterpret_cast<const float4*>(ep.gate + ti.n0 + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) gv[j] = __ldg(g4 + j);
+          const bool got = mbar_wait(bar(c), par(c), abort_flag, &s_gemm_status);
           tmem_ld_wait(r);
           if (!got) {
             // another role gave up: let the x loads this warp issued land
             // before the CTA leaves (their bytes target this CTA's buffers)
             if (lane == 0)
-              for (int d = c; d < issued; ++d)
-                mbar_wait_drain(&xb[(xu + d) % NB], static_cast<uint32_t>((xu + d) / NB) & 1u);
+              for (int d = c; d < issued; ++d) mbar_wait_drain(bar(d), par(d));
             __syncwarp();
             eok = false;
             break;
           }
+          psum(r, 32 * c);
           f8_scale<OP>(r, sa, ep.sw, ti.n0 + 32 * c);
-          float4* xs = reinterpret_cast<float4*>(eb + (u % NB) * 4096 + lane * 128);
-          const float4* g4 = reinterpret_cast<const float4*>(ep.gate + ti.n0 + 32 * c);
+          // every load of the chunk before any store (a generic store would
+          // otherwise order each later load behind it)
+          float4* xs = reinterpret_cast<float4*>(buf(c) + lane * 128);
+          float4 xv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xv[j] = xs[j ^ (lane & 7)];  // chunk j of row `lane` under the 128-byte swizzle
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int pj = j ^ (lane & 7);  // 16-byte chunk j of row `lane` under the 128-byte swizzle
-            float4 v = xs[pj];
-            const float4 gv = __ldg(g4 + j);
-            v.x = fmaf(gv.x, __uint_as_float(r[4 * j + 0]), v.x);
-            v.y = fmaf(gv.y, __uint_as_float(r[4 * j + 1]), v.y);
-            v.z = fmaf(gv.z, __uint_as_float(r[4 * j + 2]), v.z);
-            v.w = fmaf(gv.w, __uint_as_float(r[4 * j + 3]), v.w);
-            xs[pj] = v;
+            xv[j].x = fmaf(gv[j].x, __uint_as_float(r[4 * j + 0]), xv[j].x);
+            xv[j].y = fmaf(gv[j].y, __uint_as_float(r[4 * j + 1]), xv[j].y);
+            xv[j].z = fmaf(gv[j].z, __uint_as_float(r[4 * j + 2]), xv[j].z);
+            xv[j].w = fmaf(gv[j].w, __uint_as_float(r[4 * j + 3]), xv[j].w);
           }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xs[j ^ (lane & 7)] = xv[j];
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmX, eb + (u % NB) * 4096, ti.n0 + 32 * c, row0);
+            tma_store_2d(&tmX, buf(c), ti.n0 + 32 * c, row0);
             bulk_commit_group();
           }
         }
-        xu += nch;
+        if (!last) xu += c1 - c0;
       } else {
-        gemm_epilogue<BN, EPI, OP>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, ti.bn, ep);
+        gemm_epilogue<BN, EPI, OP>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, o0, o1, ep, psum);
       }
       tc_fence_before();
       __syncwarp();
@@ -606,15 +780,17 @@ cudaError_t make_gemm_plan(GemmPlan* p, int epi, int dt, int M, int N, int K, co
   p->gate = gate;
   p->qkv = QkvEpi{};
   p->f8 = false;
+  p->part = nullptr;
+  p->part_bytes = 0;
+  p->flags = nullptr;
+  p->epoch = 1;
+  p->parts_out = nullptr;
   p->sa = p->sw = nullptr;
   p->bn = (N % 256 == 0) ? 256 : 128;
   cudaError_t e = encode_2d(&p->tmA, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, mt);
   if (e != cudaSuccess) return e;
-  // each CTA of a cluster loads half of the B tile (and a quarter in the
-  // split tail)
+  // each CTA of a cluster loads half of the B tile
   e = encode_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 2, mt);
-  if (e != cudaSuccess) return e;
-  e = encode_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K) * 2, kBK, p->bn / 4, mt);
   if (e != cudaSuccess) return e;
   return encode_x_map(p);
 }
@@ -631,6 +807,11 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
   p->gate = gate;
   p->qkv = QkvEpi{};
   p->f8 = true;
+  p->part = nullptr;
+  p->part_bytes = 0;
+  p->flags = nullptr;
+  p->epoch = 1;
+  p->parts_out = nullptr;
   p->sa = sa;
   p->sw = sw;
   p->bn = 256;
@@ -638,9 +819,12 @@ cudaError_t make_gemm_plan_f8(GemmPlan* p, int epi, int M, int N, int K, const u
   if (e != cudaSuccess) return e;
   e = encode_2d(&p->tmB, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 2, MAP_U8);
   if (e != cudaSuccess) return e;
-  e = encode_2d(&p->tmBh, B, K, N, static_cast<uint64_t>(K), 128, p->bn / 4, MAP_U8);
-  if (e != cudaSuccess) return e;
   return encode_x_map(p);
+}
+
+size_t gemm_split_bytes(int bn, int tail_tiles, int parts) {
+  // one [bn][32] f32 slab per (tail tile, part, CTA rank, epilogue warp)
+  return parts > 1 ? static_cast<size_t>(tail_tiles) * parts * 8 * bn * 32 * sizeof(float) : 0;
 }
 
 // Pair rows per raster group: all of them while the whole A operand fits
@@ -683,18 +867,30 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   const int max_clusters = init->clusters;
   const int num_mp = ((p.M + kBM - 1) / kBM + 1) / 2;
   const int pairs = num_mp * (p.N / BN);
-  // split the pairs of a partial last wave that is at most half full
-  int nfull = pairs, total = pairs;
+  const int nk = p.K / (OP == kOpF8 ? 128 : kBK);
+  // a partial last wave of rem tiles runs as rem x parts K-split items in
+  // one shorter wave (parts <= max_clusters / rem, a power of two that
+  // splits the tile into owned column ranges the epilogue can finish alone:
+  // whole 128-column heads / gate-up blocks for QKV and SWIGLU, 32 columns
+  // otherwise), when the caller gave room for the partials and the flags
+  int parts = 1;
   const int rem = pairs % max_clusters;
-  if (BN == 256 && pairs > max_clusters && rem != 0 && 2 * rem <= max_clusters) {
-    nfull = pairs - rem;
-    total = nfull + 2 * rem;
+  if (pairs > max_clusters && rem != 0 && p.part != nullptr && p.flags != nullptr) {
+    constexpr int kOwnMin = (EPI == EPI_QKV || EPI == EPI_QKV_KV || EPI == EPI_SWIGLU) ? 128 : 32;
+    const int lim = std::min(std::min(max_clusters / rem, nk), std::min(kMaxKParts, BN / kOwnMin));
+    while (parts * 2 <= lim) parts *= 2;
+    while (parts > 1 && (gemm_split_bytes(BN, rem, parts) > p.part_bytes ||
+                         static_cast<size_t>(rem) * parts * 8 * sizeof(int) > kGemmFlagBytes))
+      parts /= 2;
   }
+  if (p.parts_out) *p.parts_out = parts;
+  const int nfull = parts > 1 ? pairs - rem : pairs;
+  const int total = nfull + (parts > 1 ? rem * parts : 0);
   const int clusters = std::min(total, max_clusters);
   const int group = raster_group(num_mp, p.K, OP == kOpF8 ? 1 : 2);
-  EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw};
-  gemm_tc_kernel<BN, EPI, OP><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmBh, p.tmX, p.M, p.N, p.K,
-                                                                  group, nfull, total, ep);
+  EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw, static_cast<float*>(p.part), p.flags, parts, p.epoch};
+  gemm_tc_kernel<BN, EPI, OP><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmX, p.M, p.N, p.K, group, nfull,
+                                                                  total, ep);
   return cudaGetLastError();
 }
 

@@ -524,6 +524,24 @@ int qi21_op_mods_prep(int32_t dim, const float* mods, float* md, void* stream);
 int qi21_op_gemm(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, const void* A,
                  const void* B, void* out, int32_t ldo, const float* gate_t, void* stream);
 
+/* qi21_op_gemm with the K-split tail that the block passes use. When the
+ * last wave of 256 x BN tile pairs fills only part of the GPU, each of its
+ * tiles is split along K into a power-of-two number of parts (at most 8,
+ * at most the resident clusters / tail tiles, and, for QI21_EPI_SWIGLU,
+ * whole 128-column gate/up blocks per part) that run side by side; part p
+ * finishes columns [p BN/P, (p+1) BN/P) of the tile after adding, in part
+ * order, the other parts' f32 partials. scratch: device, 256-byte aligned,
+ * scratch_bytes >= 4096; its first 4096 bytes hold the merge flags (zeroed
+ * by this call, on the stream), the rest the partials (tail tiles x parts x
+ * BN x 1 KB); with too little room the call uses fewer parts, down to none.
+ * *parts_out (host, may be NULL) receives the part count used (1: no
+ * split). The results differ from qi21_op_gemm's only in the order of the
+ * f32 additions of split tiles. Errors as qi21_op_gemm, plus
+ * QI21_ERR_WORKSPACE for a null, short or misaligned scratch. */
+int qi21_op_gemm_split(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, const void* A,
+                       const void* B, void* out, int32_t ldo, const float* gate_t, void* scratch,
+                       size_t scratch_bytes, int32_t* parts_out, void* stream);
+
 /* In place on the panel T [rows][3H] (q in columns [0, H), k in [H, 2H)):
  * per (row, head) RMSNorm * norm_q (or norm_k) over 128 values, then the
  * interleaved RoPE of pairs (2j, 2j+1) by the row's cos/sin [rows][64]

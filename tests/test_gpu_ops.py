@@ -256,31 +256,110 @@ def test_attention_prefill_mask(segs):
         np.testing.assert_allclose(got[0], panel[0, 2 * H:].astype(np.float64), atol=2 * U16 * 4)
 
 
-@pytest.mark.parametrize("epi", ["resid", "swiglu"])
-def test_gemm_partial_last_wave_split(epi):
-    # 4096 x 4096 (512 tiles of 128 x 256) and 4096 x 24576 (3072 tiles): the
-    # tiles of the partial last wave run as 128 x 128 halves; sampled rows
-    # cover the last M tiles, where the split tiles sit
-    M, K = 4096, 512
-    rows = np.array([0, 127, 2048, 2175, 3968, 4000, 4095])
-    A = S.op_tensor(10, 1, 0, (M, K), 1.0).astype(np.float16)
-    a = A[rows].astype(np.float64)
-    if epi == "resid":
-        N = 4096
-        Bw = S.op_tensor(10, 1, 1, (N, K), K ** -0.5).astype(np.float16)
-        x0 = S.op_tensor(10, 1, 2, (M, N), 1.0)
-        gt = np.tanh(S.op_tensor(10, 1, 3, (N,), 0.1))
-        xd = T(x0)
-        q.op_gemm(q.EPI_RESID, T(A), T(Bw), xd, gate_t=T(gt))
-        got = xd[torch.from_numpy(rows).cuda()].cpu().numpy()
-        ref = x0[rows] + gt.astype(np.float64) * (a @ Bw.astype(np.float64).T)
-        assert np.max(np.abs(got - ref)) < 1e-4
+def _expected_parts(epi, M, N, K, clusters):
+    """The documented part count of qi21_op_gemm_split with ample scratch:
+    the tiles of a partial last wave (pairs of 256 rows x BN columns) split
+    into the largest power of two <= min(8, clusters // tail tiles, k-blocks,
+    BN / owner width), owner width 128 for SWIGLU, else 32."""
+    bn = 256 if N % 256 == 0 else 128
+    pairs = ((M + 127) // 128 + 1) // 2 * (N // bn)
+    rem = pairs % clusters
+    if pairs <= clusters or rem == 0:
+        return 1
+    lim = min(8, clusters // rem, K // 64, bn // (128 if epi == "swiglu" else 32))
+    p = 1
+    while p * 2 <= lim:
+        p *= 2
+    return p
+
+
+def _split_case(epi, dtype, M, N, K, seed):
+    A = S.op_tensor(11, seed, 0, (M, K), 1.0).astype(np.float32)
+    Bw = S.op_tensor(11, seed, 1, (N, K), K ** -0.5).astype(np.float32)
+    if dtype == "bf16":
+        A, Bw = S.bf16_values(S.bf16_bits(A)), S.bf16_values(S.bf16_bits(Bw))
+        tA, tB = T(A).to(torch.bfloat16), T(Bw).to(torch.bfloat16)
     else:
-        I = 12288
-        G = S.op_tensor(10, 2, 1, (I, K), K ** -0.5).astype(np.float16)
-        Up = S.op_tensor(10, 2, 2, (I, K), K ** -0.5).astype(np.float16)
-        out = torch.empty((M, I), dtype=torch.float16, device="cuda")
-        q.op_gemm(q.EPI_SWIGLU, T(A), T(_interleave_w13(G, Up)), out)
-        got = out[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
-        ref = O.silu(a @ G.astype(np.float64).T) * (a @ Up.astype(np.float64).T)
-        assert np.all(np.abs(got - ref) <= 2 * U16 * np.abs(ref) + 2e-3)
+        A, Bw = A.astype(np.float16), Bw.astype(np.float16)
+        tA, tB = T(A), T(Bw)
+    return A, Bw, tA, tB
+
+
+# (epilogue, operand type, M, N, K): tail tiles of 4, 16, 28 and 14 pairs
+# (parts 8, 4, 2 and 4 on 76 resident clusters), a 128-column tile, the
+# SWIGLU cap at two parts and at one (128-column tiles)
+SPLIT_CASES = [
+    ("resid", "f16", 2500, 2048, 1024),
+    ("f32", "f16", 5788, 1024, 768),
+    ("f16", "f16", 3251, 2048, 512),
+    ("swiglu", "f16", 2500, 2048, 1024),
+    ("resid", "bf16", 2500, 1152, 512),
+    ("swiglu", "bf16", 2500, 1152, 512),
+    ("resid", "f16", 4096, 4096, 4096),
+]
+
+
+@pytest.mark.parametrize("epi,dtype,M,N,K", SPLIT_CASES)
+def test_gemm_k_split_tail(epi, dtype, M, N, K):
+    # the K-split tail against the oracle's f64 products; against the
+    # unsplit GEMM (the same sums in another order: f32 rounding apart); two
+    # split runs bit-identical; with no room for partials it is the unsplit
+    # GEMM bit for bit
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    A, Bw, tA, tB = _split_case(epi, dtype, M, N, K, M + N + K)
+    E = {"resid": q.EPI_RESID, "f32": q.EPI_F32, "f16": q.EPI_F16, "swiglu": q.EPI_SWIGLU}[epi]
+    scratch = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    cols = N // 2 if epi == "swiglu" else N
+    odt = torch.float32 if epi in ("resid", "f32") else tA.dtype
+    x0 = S.op_tensor(11, M, 2, (M, cols), 1.0) if epi == "resid" else None
+    gt = T(np.tanh(S.op_tensor(11, M, 3, (N,), 0.1))) if epi == "resid" else None
+
+    def run(split, room=64 << 20):
+        out = T(x0) if epi == "resid" else torch.zeros((M, cols), dtype=odt, device="cuda")
+        if split:
+            parts = q.op_gemm_split(E, tA, tB, out, scratch[:room], gate_t=gt)
+        else:
+            q.op_gemm(E, tA, tB, out, gate_t=gt)
+            parts = 1
+        return host(out.float()).astype(np.float64), parts
+
+    got, parts = run(True)
+    assert parts == _expected_parts(epi, M, N, K, clusters)
+    rows = np.arange(M) if M * N * K <= 8e9 else np.array([0, 1, 255, 256, 2047, 3840, 3968, 4095])
+    a = A[rows].astype(np.float64)
+    if epi == "swiglu":
+        G, Up = np.empty((N // 2, K)), np.empty((N // 2, K))
+        for j in range(N // 128):  # the interleaved plane: 64 gate rows, then 64 up rows
+            G[64 * j:64 * j + 64] = Bw[128 * j:128 * j + 64]
+            Up[64 * j:64 * j + 64] = Bw[128 * j + 64:128 * j + 128]
+        ref = O.silu(a @ G.T) * (a @ Up.T)
+    else:
+        ref = a @ Bw.astype(np.float64).T
+        if epi == "resid":
+            ref = x0[rows] + np.tanh(S.op_tensor(11, M, 3, (N,), 0.1)).astype(np.float64) * ref
+    g = got[rows]
+    u = U16 if dtype == "f16" else 2.0 ** -8
+    if epi in ("resid", "f32"):
+        assert rel_l2(g, ref) < 1e-5
+    else:
+        assert np.all(np.abs(g - ref) <= 2 * u * np.abs(ref) + 2e-3)
+    plain, _ = run(False)
+    if epi in ("resid", "f32"):
+        assert np.max(np.abs(got - plain)) <= 1e-5 * np.max(np.abs(plain))
+    else:  # one output rounding apart at most
+        assert np.all(np.abs(got - plain) <= 2 * u * np.abs(plain) + 1e-6)
+    again, _ = run(True)
+    np.testing.assert_array_equal(again, got)
+    none, p1 = run(True, room=4096)
+    assert p1 == 1
+    np.testing.assert_array_equal(none, plain)
+
+
+def test_gemm_split_rejects_bad_scratch():
+    A, Bw, tA, tB = _split_case("f16", "f16", 256, 256, 64, 1)
+    out = torch.empty((256, 256), dtype=torch.float16, device="cuda")
+    scratch = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    for bad in (scratch[:100], scratch[16:]):
+        with pytest.raises(q.Qi21Error) as e:
+            q.op_gemm_split(q.EPI_F16, tA, tB, out, bad)
+        assert e.value.code == -8
