@@ -153,13 +153,12 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 struct PartSum {
   const float* st;  // this warp's staged partials [other part][w][32], null if none
   int parts, own, w, o0;
-  // kTwo: the caller never splits in more than two parts (128-column owners
-  // of a 256-column tile)
-  template <bool kTwo = false>
+  // kMaxP: the most parts the caller's epilogue splits into
+  template <int kMaxP>
   __device__ __forceinline__ void add(uint32_t (&r)[32], int col) const {
     if (st == nullptr) return;
     const float* b = st + static_cast<size_t>(col - o0) * 32 + (threadIdx.x & 31);
-    if (kTwo || parts == 2) {  // one other part; a + b == b + a, whichever part owns
+    if (kMaxP == 2 || parts == 2) {  // one other part; a + b == b + a, whichever part owns
 #pragma unroll
       for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + b[e * 32]);
       return;
@@ -169,12 +168,30 @@ struct PartSum {
     for (int e = 0; e < 32; ++e) {
       const float a = __uint_as_float(r[e]);
       float s = own == 0 ? a : b[e * 32];
-      for (int pp = 1; pp < parts; ++pp) s += pp == own ? a : b[(pp < own ? pp : pp - 1) * slot + e * 32];
+#pragma unroll
+      for (int pp = 1; pp < kMaxP; ++pp)
+        if (pp < parts) s += pp == own ? a : b[(pp < own ? pp : pp - 1) * slot + e * 32];
       r[e] = __float_as_uint(s);
     }
   }
-  __device__ __forceinline__ void operator()(uint32_t (&r)[32], int col) const { add<false>(r, col); }
+  __device__ __forceinline__ void operator()(uint32_t (&r)[32], int col) const { add<kMaxKParts>(r, col); }
 };
+
+// Owner width of a split tail tile: the qkv epilogue normalises whole
+// 128-column heads and SwiGLU pairs 64 gate with 64 up columns, so their
+// owners take 128 columns; the other epilogues take 32-column chunks.
+// Parts: at most 2 for both (on a 128-column tile one owner and one part
+// that only contributes its partial). Four SwiGLU parts (two owners and
+// two contributors per 256-column tile) measured slower than two on the
+// gate/up projection: the extra partial traffic outweighs the shorter tail.
+template <int EPI>
+constexpr int split_own_min() {
+  return (EPI == EPI_QKV || EPI == EPI_QKV_KV || EPI == EPI_SWIGLU) ? 128 : 32;
+}
+template <int EPI>
+constexpr int split_max_parts() {
+  return split_own_min<EPI>() == 128 ? 2 : kMaxKParts;
+}
 
 // FP8: 32 accumulator columns starting at column `col` times sa sw[col + i]
 template <int OP>
@@ -215,8 +232,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
         tmem_ld32(tbase + p * 128 + 64 + c * 32, u);
         tmem_ld_wait(g);
         tmem_ld_wait(u);
-        padd.add<true>(g, p * 128 + c * 32);
-        padd.add<true>(u, p * 128 + 64 + c * 32);
+        padd.add<2>(g, p * 128 + c * 32);
+        padd.add<2>(u, p * 128 + 64 + c * 32);
         f8_scale<OP>(g, sa, ep.sw, n0 + p * 128 + c * 32);
         f8_scale<OP>(u, sa, ep.sw, n0 + p * 128 + 64 + c * 32);
         if (live) {
@@ -257,7 +274,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) padd.add<true>(r[c], hc * 128 + c * 32);
+      for (int c = 0; c < 4; ++c) padd.add<2>(r[c], hc * 128 + c * 32);
       if (!live) continue;
 #pragma unroll
       for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
@@ -556,10 +573,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
       // accumulator columns whose outputs this item writes: all of them, or
       // for part p of a K-split tail tile (always a cluster's last item)
-      // columns [p w, (p + 1) w)
+      // columns [p w, (p + 1) w), w = max(BN / parts, owner width); parts
+      // past the last owner only contribute partials
       const int P = ti.part >= 0 ? ep.parts : 1;
-      const int w = ti.bn / P;
-      const int o0 = ti.part >= 0 ? ti.part * w : 0, o1 = o0 + w;
+      const int w = max(ti.bn / P, split_own_min<EPI>());
+      const int o0 = ti.part >= 0 ? min(ti.part * w, ti.bn) : 0, o1 = min(o0 + w, ti.bn);
+      const bool owner = o1 > o0;
       // the last item's x chunks (EPI_RESID) sit after the staged partials
       const int xoff = (P - 1) * w * 128;
       const int row0 = (2 * ti.mp + rank) * kBM + q * 32;  // this warp's first row
@@ -593,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           *abort_flag = 1;
           atomicOr(&s_gemm_status, kStatusTimeout);
         }
-        if (lane == 0)
+        if (owner && lane == 0)
           for (int pp = 0; pp < P && got; ++pp)
             if (pp != ti.part) got = wait_flag(ep.flags + sbase + pp * 8, ep.epoch, abort_flag, &s_gemm_status);
         __syncwarp();
@@ -605,19 +624,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           eok = false;
           break;
         }
-        __threadfence();
-        float* st = reinterpret_cast<float*>(wst);
-        int slot = 0;
-        for (int pp = 0; pp < P; ++pp) {
-          if (pp == ti.part) continue;
-          const float* src = ep.part + (sbase + pp * 8) * slab + static_cast<size_t>(o0) * 32;
-          float* dst = st + static_cast<size_t>(slot) * w * 32;
-          for (int i = lane; i < w * 8; i += 32) cp_async16(dst + 4 * i, src + 4 * i);
-          ++slot;
+        if (owner) {
+          __threadfence();
+          float* st = reinterpret_cast<float*>(wst);
+          int slot = 0;
+          for (int pp = 0; pp < P; ++pp) {
+            if (pp == ti.part) continue;
+            const float* src = ep.part + (sbase + pp * 8) * slab + static_cast<size_t>(o0) * 32;
+            float* dst = st + static_cast<size_t>(slot) * w * 32;
+            for (int i = lane; i < w * 8; i += 32) cp_async16(dst + 4 * i, src + 4 * i);
+            ++slot;
+          }
+          cp_async_commit_wait_all();
+          __syncwarp();
+          psum = PartSum{st, P, ti.part, w, o0};
         }
-        cp_async_commit_wait_all();
-        __syncwarp();
-        psum = PartSum{st, P, ti.part, w, o0};
       }
       if constexpr (EPI == EPI_RESID) {
         // x += tanh(g) acc for this warp's 32 rows, 32 columns at a time:
@@ -869,15 +890,17 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   const int pairs = num_mp * (p.N / BN);
   const int nk = p.K / (OP == kOpF8 ? 128 : kBK);
   // a partial last wave of rem tiles runs as rem x parts K-split items in
-  // one shorter wave (parts <= max_clusters / rem, a power of two that
-  // splits the tile into owned column ranges the epilogue can finish alone:
-  // whole 128-column heads / gate-up blocks for QKV and SWIGLU, 32 columns
-  // otherwise), when the caller gave room for the partials and the flags
+  // one shorter wave: parts a power of two <= max_clusters / rem and <= the
+  // k-blocks; with 32-column owners at most 8 and BN / 32 (every part owns
+  // columns), with 128-column owners (QKV, SWIGLU) at most 2 (on a
+  // 128-column tile the second part only contributes its partial); only
+  // when the caller gave room for the partials and the flags
   int parts = 1;
   const int rem = pairs % max_clusters;
   if (pairs > max_clusters && rem != 0 && p.part != nullptr && p.flags != nullptr) {
-    constexpr int kOwnMin = (EPI == EPI_QKV || EPI == EPI_QKV_KV || EPI == EPI_SWIGLU) ? 128 : 32;
-    const int lim = std::min(std::min(max_clusters / rem, nk), std::min(kMaxKParts, BN / kOwnMin));
+    const int cap = split_own_min<EPI>() == 128 ? split_max_parts<EPI>() : std::min(kMaxKParts, BN / 32);
+    static_assert(split_max_parts<EPI>() <= kMaxKParts, "part cap");
+    const int lim = std::min(std::min(max_clusters / rem, nk), cap);
     while (parts * 2 <= lim) parts *= 2;
     while (parts > 1 && (gemm_split_bytes(BN, rem, parts) > p.part_bytes ||
                          static_cast<size_t>(rem) * parts * 8 * sizeof(int) > kGemmFlagBytes))

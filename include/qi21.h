@@ -526,11 +526,13 @@ int qi21_op_gemm(int32_t dtype, int32_t epi, int32_t M, int32_t N, int32_t K, co
 
 /* qi21_op_gemm with the K-split tail that the block passes use. When the
  * last wave of 256 x BN tile pairs fills only part of the GPU, each of its
- * tiles is split along K into a power-of-two number of parts (at most 8,
- * at most the resident clusters / tail tiles, and, for QI21_EPI_SWIGLU,
- * whole 128-column gate/up blocks per part) that run side by side; part p
- * finishes columns [p BN/P, (p+1) BN/P) of the tile after adding, in part
- * order, the other parts' f32 partials. scratch: device, 256-byte aligned,
+ * tiles is split along K into a power-of-two number of parts (at most the
+ * resident clusters / tail tiles and the k-blocks; at most 8 and BN/32,
+ * or for QI21_EPI_SWIGLU at most 2) that run side by side; part p finishes
+ * columns [p W, (p+1) W) of the tile (W = BN/P, for QI21_EPI_SWIGLU at
+ * least one 128-column gate/up block, a part past the last block only
+ * contributing its partial) after adding, in part order, every part's f32
+ * partial. scratch: device, 256-byte aligned,
  * scratch_bytes >= 4096; its first 4096 bytes hold the merge flags (zeroed
  * by this call, on the stream), the rest the partials (tail tiles x parts x
  * BN x 1 KB); with too little room the call uses fewer parts, down to none.

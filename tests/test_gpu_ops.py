@@ -259,14 +259,16 @@ def test_attention_prefill_mask(segs):
 def _expected_parts(epi, M, N, K, clusters):
     """The documented part count of qi21_op_gemm_split with ample scratch:
     the tiles of a partial last wave (pairs of 256 rows x BN columns) split
-    into the largest power of two <= min(8, clusters // tail tiles, k-blocks,
-    BN / owner width), owner width 128 for SWIGLU, else 32."""
+    into the largest power of two <= min(clusters // tail tiles, k-blocks,
+    cap), cap 2 for SWIGLU (128-column owners; on a 128-column tile the
+    second part only contributes), else min(8, BN / 32)."""
     bn = 256 if N % 256 == 0 else 128
     pairs = ((M + 127) // 128 + 1) // 2 * (N // bn)
     rem = pairs % clusters
     if pairs <= clusters or rem == 0:
         return 1
-    lim = min(8, clusters // rem, K // 64, bn // (128 if epi == "swiglu" else 32))
+    cap = 2 if epi == "swiglu" else min(8, bn // 32)
+    lim = min(cap, clusters // rem, K // 64)
     p = 1
     while p * 2 <= lim:
         p *= 2
@@ -286,8 +288,9 @@ def _split_case(epi, dtype, M, N, K, seed):
 
 
 # (epilogue, operand type, M, N, K): tail tiles of 4, 16, 28 and 14 pairs
-# (parts 8, 4, 2 and 4 on 76 resident clusters), a 128-column tile, the
-# SWIGLU cap at two parts and at one (128-column tiles)
+# (parts 8, 4, 2 and 4 on 76 resident clusters), a 128-column tile, SWIGLU
+# at its cap of two parts (two owners on 256-column tiles; one owner and
+# one contributor on 128-column tiles)
 SPLIT_CASES = [
     ("resid", "f16", 2500, 2048, 1024),
     ("f32", "f16", 5788, 1024, 768),
@@ -295,6 +298,7 @@ SPLIT_CASES = [
     ("swiglu", "f16", 2500, 2048, 1024),
     ("resid", "bf16", 2500, 1152, 512),
     ("swiglu", "bf16", 2500, 1152, 512),
+    ("swiglu", "f16", 3251, 2048, 512),
     ("resid", "f16", 4096, 4096, 4096),
 ]
 
@@ -346,8 +350,8 @@ def test_gemm_k_split_tail(epi, dtype, M, N, K):
     plain, _ = run(False)
     if epi in ("resid", "f32"):
         assert np.max(np.abs(got - plain)) <= 1e-5 * np.max(np.abs(plain))
-    else:  # one output rounding apart at most
-        assert np.all(np.abs(got - plain) <= 2 * u * np.abs(plain) + 1e-6)
+    else:  # one output rounding apart, plus the f32 reordering of O(1) sums
+        assert np.all(np.abs(got - plain) <= 2 * u * np.abs(plain) + 1e-5)
     again, _ = run(True)
     np.testing.assert_array_equal(again, got)
     none, p1 = run(True, room=4096)
