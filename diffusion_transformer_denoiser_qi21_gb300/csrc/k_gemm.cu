@@ -400,6 +400,7 @@ struct TileInfo {
   int kb0, kb1;  // k-blocks of this item
   int part;      // -1 whole tile, else the part of a split tail tile
   int tail;      // index of the tail tile (split tiles only)
+  bool rev;      // load the k-blocks from kb1 - 1 down (whole tiles of odd waves)
 };
 
 __device__ __forceinline__ void raster(int f, int num_mp, int nN, int G, int& mp, int& nb) {
@@ -412,18 +413,22 @@ __device__ __forceinline__ void raster(int f, int num_mp, int nN, int G, int& mp
   nb = r / gs;
 }
 
+// Whole tiles of odd waves (t / nclusters odd) walk K downwards: a wave
+// then starts on the k-slices of the A / B panels that the previous wave
+// read last, which are the ones still in L2.
 template <int BN>
-__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, int nfull, int parts, int nk) {
+__device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, int nfull, int parts, int nk,
+                                            int nclusters) {
   int mp, nb;
   if (t < nfull) {
     raster(t, num_mp, nN, G, mp, nb);
-    return TileInfo{mp, nb * BN, BN, 0, nk, -1, 0};
+    return TileInfo{mp, nb * BN, BN, 0, nk, -1, 0, ((t / nclusters) & 1) != 0};
   }
   const int u = t - nfull;
   const int tail = u / parts;
   const int part = u - tail * parts;
   raster(nfull + tail, num_mp, nN, G, mp, nb);
-  return TileInfo{mp, nb * BN, BN, part * nk / parts, (part + 1) * nk / parts, part, tail};
+  return TileInfo{mp, nb * BN, BN, part * nk / parts, (part + 1) * nk / parts, part, tail, false};
 }
 
 template <int BN, int EPI, int OP>
@@ -489,7 +494,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
+        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk, nclusters);
         const int m0 = (2 * ti.mp + rank) * kBM;
         const int bh = BN / 2;  // B rows this CTA holds
         // the even CTA's barrier counts both CTAs' A and B bytes
@@ -502,8 +507,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           uint8_t* sa = smem + s * C::kStageBytes;
           const uint32_t fb = mapa_rank(&full[s], 0);
           if (leader) mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d_pair(sa, &tmA, fb, kb * kKE, m0);
-          tma_load_2d_pair(sa + C::kABytes, &tmB, fb, kb * kKE, ti.n0 + rank * bh);
+          const int kc = ti.rev ? ti.kb0 + ti.kb1 - 1 - kb : kb;  // the k-block loaded into this stage
+          tma_load_2d_pair(sa, &tmA, fb, kc * kKE, m0);
+          tma_load_2d_pair(sa + C::kABytes, &tmB, fb, kc * kKE, ti.n0 + rank * bh);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -519,7 +525,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       int it = 0;
       bool ok = true;
       for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
-        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
+        const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk, nclusters);
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, &s_gemm_status)) break;
@@ -561,7 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint8_t* const wst = smem + q * C::kTailWarpBytes;
     uint64_t* const xl = xbar + 4 * C::kXBufs + 8 * q;
     for (int t = cluster; t < num_tiles && eok; t += nclusters, ++it) {
-      const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk);
+      const TileInfo ti = tile_at<BN>(t, num_mp, nN, group, nfull, ep.parts, nk, nclusters);
       const bool last = t + nclusters >= num_tiles;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
