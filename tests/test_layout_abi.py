@@ -103,6 +103,27 @@ def test_geometry_ok_and_sizes(dtype):
     assert q.workspace_bytes(g, M) < M * per_row + fixed + 8 * 256
 
 
+def test_empty_inputs_are_no_ops():
+    # zero rows (queries, codes) are valid and enqueue nothing: every
+    # single-operation entry point returns 0 before it looks at a pointer
+    # or touches the device (no CUDA context is needed here)
+    lib = q.load()
+    for dt in (0, 1):
+        assert lib.qi21_op_gemm(dt, 0, 0, 128, 64, None, None, None, 128, None, None) == 0
+        assert lib.qi21_op_gemm(dt, 2, 0, 256, 64, None, None, None, 256, None, None) == 0  # residual, no gate
+        assert lib.qi21_op_rowop(dt, 0, 256, 1e-6, None, None, None, None, None, None) == 0
+        assert lib.qi21_op_qkrope(dt, 0, 2, 1e-6, None, None, None, None, None, None) == 0
+        assert lib.qi21_op_attention(dt, 0, 2, None, None, 0, 0, None, None, None) == 0
+        assert lib.qi21_op_gemm_split(dt, 0, 0, 128, 64, None, None, None, 128, None, None, 0, None, None) == 0
+    assert lib.qi21_op_kvcopy(0, 256, None, None, None) == 0
+    assert lib.qi21_op_quant_rows(0, 256, None, None, None, None) == 0
+    assert lib.qi21_op_rowop_fp8(0, 256, 1e-6, None, None, None, None, None) == 0
+    assert lib.qi21_op_gemm_fp8(1, 0, 256, 128, None, None, None, None, None, 256, None, None) == 0
+    # negative sizes are refused
+    assert lib.qi21_op_gemm(0, 0, -1, 128, 64, None, None, None, 128, None, None) == -2
+    assert lib.qi21_op_attention(0, -1, 2, None, None, 0, 0, None, None, None) == -2
+
+
 def test_device_entry_points_reject_bad_args_before_touching_the_device():
     lib = q.load()
     g = q.geom(256, 2, 768, 1)
