@@ -34,9 +34,6 @@
 //   warp 0     TMA producer (both CTAs): A 128x64 and B (BN/2)x64 tiles
 //              (128-byte swizzle) into a 6-stage ring; the loads of both CTAs
 //              complete on the even CTA's "full" mbarrier
-// Tiles are visited in groups of G pair rows (column blocks outer, the
-// pair rows of a group inner), G chosen on the host so that the group's A
-// rows stay in L2 while its column blocks stream past.
 //   warp 1     TMEM allocation (jointly, both CTAs); in the even CTA one
 //              thread issues the pair MMAs (M=256, N=BN, K=16) and commits
 //              that release a stage / publish an accumulator in both CTAs
@@ -44,6 +41,15 @@
 //              fused op, 128-bit stores; two TMEM accumulators so the
 //              epilogue of tile i overlaps the MMAs of tile i+1; each warp
 //              reports "accumulator free" to the even CTA.
+// Schedule (tile_at): tiles in groups of G pair rows (column blocks outer,
+// the pair rows of a group inner), G chosen on the host so that the group's
+// A rows stay in L2 while its column blocks stream past; whole tiles of odd
+// waves load their k-blocks top down (a wave starts on the k-slices its
+// predecessor read last); a partial last wave is split along K into
+// column-owned parts that run side by side and merge their f32 partials
+// through global scratch (the K-split tail). A cluster's last item stages
+// its epilogue data (x chunks, other parts' partials) in the then idle
+// operand ring.
 #include <algorithm>
 #include <cstdio>
 
