@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, os.path.join(HERE, "golden"))
 import make_fullwidth_golden as G  # noqa: E402
 
-NAMES = ["step32_cond4114_n4096", "step32_n16384", "cfg_pair32_n1024"]
+NAMES = ["step32_cond4114_n4096", "step32_n16384", "cfg_pair32_n1024", "step32_cond4114_n4096_bf16"]
 
 
 @pytest.mark.parametrize("name", NAMES)

@@ -14,7 +14,8 @@ source hash or input summary no longer matches is skipped with the
 reason, never trusted.
 
 Bar: rel L2 <= 2e-3 for every block output (step and prefill) and for the
-cache, on the stored rows and on the sketches.
+cache (6e-3 for the bf16 cache: one bf16 rounding of a stored value), on
+the stored rows and on the sketches.
 """
 import os
 import sys
@@ -57,9 +58,26 @@ def layers32():
 
 @pytest.mark.parametrize("name", ["step32_cond4114_n4096", "step32_n16384", "cfg_pair32_n1024"])
 def test_full_width_32_layers_end_to_end(name, layers32):
+    _end_to_end(name, layers32, X_TOL, KV_TOL)
+
+
+def test_full_width_bf16_end_to_end():
+    # the bench workload in bf16 (weights, activation rows and cache): the
+    # same bar on the block outputs; the cache within bf16's one-rounding
+    # bar (6e-3: relative RMS 2^-8 / sqrt(3) of a stored value)
+    name = "step32_cond4114_n4096_bf16"
+    _golden(name)
+    w = S.WORKLOADS[name]
+    layers = D.upload_layers(w, D.geom_of(w))
+    _end_to_end(name, layers, X_TOL, 6e-3)
+    del layers
+    torch.cuda.empty_cache()
+
+
+def _end_to_end(name, layers, x_tol, kv_tol):
     w = S.WORKLOADS[name]
     meta, arr = _golden(name)
-    run = DeviceRun(w, layers=layers32)
+    run = DeviceRun(w, layers=layers)
     H, L, n = w.dim, w.layers, w.n_target
     K = meta["sketch_k"]
     B = S.sketch(H, K, 1)
@@ -81,10 +99,10 @@ def test_full_width_32_layers_end_to_end(name, layers32):
                 e_pre = rel_l2(G.sketch_of(run.pre_x(layer, s), Ap, B), arr[f"pre_sketch_s{s}"][layer])
             print(f"{name} seq {s} layer {layer}: step rows {e_rows:.2e} sketch {e_sk:.2e}, "
                   f"prefill {e_pre:.2e}, K {e_k:.2e} V {e_v:.2e}")
-            assert e_rows <= X_TOL, f"seq {s} layer {layer}: sampled rows rel L2 {e_rows:.3e}"
-            assert e_sk <= X_TOL, f"seq {s} layer {layer}: step sketch rel L2 {e_sk:.3e}"
-            assert e_pre <= X_TOL, f"seq {s} layer {layer}: prefill sketch rel L2 {e_pre:.3e}"
-            assert e_k <= KV_TOL and e_v <= KV_TOL, f"seq {s} layer {layer}: K {e_k:.3e} V {e_v:.3e}"
+            assert e_rows <= x_tol, f"seq {s} layer {layer}: sampled rows rel L2 {e_rows:.3e}"
+            assert e_sk <= x_tol, f"seq {s} layer {layer}: step sketch rel L2 {e_sk:.3e}"
+            assert e_pre <= x_tol, f"seq {s} layer {layer}: prefill sketch rel L2 {e_pre:.3e}"
+            assert e_k <= kv_tol and e_v <= kv_tol, f"seq {s} layer {layer}: K {e_k:.3e} V {e_v:.3e}"
             worst["step_rows"] = max(worst["step_rows"], e_rows)
             worst["step"] = max(worst["step"], e_sk)
             worst["prefill"] = max(worst["prefill"], e_pre)
