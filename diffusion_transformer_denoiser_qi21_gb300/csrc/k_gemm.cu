@@ -215,6 +215,20 @@ __device__ __forceinline__ void f8_scale(uint32_t (&r)[32], float sa, const floa
   }
 }
 
+// 32 bytes from / to global memory in one access per thread (a whole
+// sector: the qkv epilogue's rows are one per thread, so a warp's accesses
+// touch 32 rows); p 32-byte aligned.
+__device__ __forceinline__ void ldg8(const float* p, float (&r)[8]) {
+  asm("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void stg8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // silu(v) = v / (1 + e^-v) with the approximate exponential and divide
 // (relative error ~2^-21, far below the 16-bit rounding of the output)
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
@@ -268,8 +282,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     for (int i = 1; i < kMaxSeq; ++i)
       if (i < qe.tabs.nsrc && row >= qe.tabs.src[i].row0) si = i;
     const size_t trow = static_cast<size_t>(live ? row - qe.tabs.src[si].row0 : 0) * 64;
-    const float4* cs4 = reinterpret_cast<const float4*>(qe.tabs.src[si].cos_ + trow);
-    const float4* sn4 = reinterpret_cast<const float4*>(qe.tabs.src[si].sin_ + trow);
+    const float* cs = qe.tabs.src[si].cos_ + trow;
+    const float* sn = qe.tabs.src[si].sin_ + trow;
 #pragma unroll 1
     for (int hc = o0 / 128; hc < o1 / 128; ++hc) {
       const int col = n0 + hc * 128;
@@ -284,24 +298,22 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
       if (!live) continue;
 #pragma unroll
       for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
-      uint4* dst = reinterpret_cast<uint4*>(out + col);
+      uint16_t* dst = out + col;
       // prefill: the same k / v values into the cache row (K at col - H, V at col - H)
-      uint4* kvd = (EPI == EPI_QKV_KV && part > 0)
-                       ? reinterpret_cast<uint4*>(static_cast<uint16_t*>(qe.kv) +
-                                                  static_cast<size_t>(row) * 2 * qe.H + (col - qe.H))
-                       : nullptr;
+      uint16_t* kvd = (EPI == EPI_QKV_KV && part > 0)
+                          ? static_cast<uint16_t*>(qe.kv) + static_cast<size_t>(row) * 2 * qe.H + (col - qe.H)
+                          : nullptr;
       if (part == 2) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = make_uint4(
-                pack2<BF>(__uint_as_float(r[c][8 * j + 0]), __uint_as_float(r[c][8 * j + 1])),
-                pack2<BF>(__uint_as_float(r[c][8 * j + 2]), __uint_as_float(r[c][8 * j + 3])),
-                pack2<BF>(__uint_as_float(r[c][8 * j + 4]), __uint_as_float(r[c][8 * j + 5])),
-                pack2<BF>(__uint_as_float(r[c][8 * j + 6]), __uint_as_float(r[c][8 * j + 7])));
-            dst[c * 4 + j] = v;
-            if constexpr (EPI == EPI_QKV_KV) kvd[c * 4 + j] = v;
+          for (int j2 = 0; j2 < 2; ++j2) {
+            uint32_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = pack2<BF>(__uint_as_float(r[c][16 * j2 + 2 * e]), __uint_as_float(r[c][16 * j2 + 2 * e + 1]));
+            stg8(dst + c * 32 + j2 * 16, v);
+            if constexpr (EPI == EPI_QKV_KV) stg8(kvd + c * 32 + j2 * 16, v);
           }
         continue;
       }
@@ -314,31 +326,33 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
           ss[e & 3] = fmaf(v, v, ss[e & 3]);
         }
       const float inv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / 128.f) + qe.eps);
+      // the norm weights (the caller's, 16-byte aligned; the same address in
+      // every lane) in 16-byte loads; the per-row tables and outputs, in
+      // the library's 256-byte aligned buffers, 32 bytes at a time
       const float4* w4 = reinterpret_cast<const float4*>(part == 0 ? qe.norm_q : qe.norm_k);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // elements 32c + 8j .. +7 = pairs 16c + 4j .. +3
-          const float4 wa = __ldg(w4 + 8 * c + 2 * j);
-          const float4 wb = __ldg(w4 + 8 * c + 2 * j + 1);
-          const float4 cv = __ldg(cs4 + 4 * c + j);
-          const float4 sv = __ldg(sn4 + 4 * c + j);
-          const float a0 = __uint_as_float(r[c][8 * j + 0]) * inv * wa.x;
-          const float b0 = __uint_as_float(r[c][8 * j + 1]) * inv * wa.y;
-          const float a1 = __uint_as_float(r[c][8 * j + 2]) * inv * wa.z;
-          const float b1 = __uint_as_float(r[c][8 * j + 3]) * inv * wa.w;
-          const float a2 = __uint_as_float(r[c][8 * j + 4]) * inv * wb.x;
-          const float b2 = __uint_as_float(r[c][8 * j + 5]) * inv * wb.y;
-          const float a3 = __uint_as_float(r[c][8 * j + 6]) * inv * wb.z;
-          const float b3 = __uint_as_float(r[c][8 * j + 7]) * inv * wb.w;
-          const uint4 v = make_uint4(pack2<BF>(a0 * cv.x - b0 * sv.x, a0 * sv.x + b0 * cv.x),
-                                     pack2<BF>(a1 * cv.y - b1 * sv.y, a1 * sv.y + b1 * cv.y),
-                                     pack2<BF>(a2 * cv.z - b2 * sv.z, a2 * sv.z + b2 * cv.z),
-                                     pack2<BF>(a3 * cv.w - b3 * sv.w, a3 * sv.w + b3 * cv.w));
-          dst[c * 4 + j] = v;
+        for (int j2 = 0; j2 < 2; ++j2) {
+          // elements 32c + 16j2 .. +15 = pairs 16c + 8j2 .. +7
+          float4 w[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) w[q4] = __ldg(w4 + 8 * c + 4 * j2 + q4);
+          float cv[8], sv[8];
+          ldg8(cs + 16 * c + 8 * j2, cv);
+          ldg8(sn + 16 * c + 8 * j2, sv);
+          uint32_t v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 wq = w[e >> 1];
+            const float w0 = (e & 1) ? wq.z : wq.x, w1 = (e & 1) ? wq.w : wq.y;
+            const float a = __uint_as_float(r[c][16 * j2 + 2 * e]) * inv * w0;
+            const float b = __uint_as_float(r[c][16 * j2 + 2 * e + 1]) * inv * w1;
+            v[e] = pack2<BF>(a * cv[e] - b * sv[e], a * sv[e] + b * cv[e]);
+          }
+          stg8(dst + c * 32 + j2 * 16, v);
           if constexpr (EPI == EPI_QKV_KV)
-            if (part == 1) kvd[c * 4 + j] = v;
+            if (part == 1) stg8(kvd + c * 32 + j2 * 16, v);
         }
       }
     }
