@@ -101,12 +101,12 @@ def class_work(w, n_rows, vis_sum):
 # capture time. Reported only while those sources are unchanged.
 NCU_TRAFFIC = {
     # class: (source file, sha256 of its sources at capture, bytes per launch)
-    "qkv": ("k_gemm.cu", "17e241cba63077e04481a436834a5dc315b286bfb7e7b0f1c63a68eb28da23f8", 241502250),
-    "o": ("k_gemm.cu", "17e241cba63077e04481a436834a5dc315b286bfb7e7b0f1c63a68eb28da23f8", 186991957),
-    "gateup": ("k_gemm.cu", "17e241cba63077e04481a436834a5dc315b286bfb7e7b0f1c63a68eb28da23f8", 339012309),
-    "down": ("k_gemm.cu", "17e241cba63077e04481a436834a5dc315b286bfb7e7b0f1c63a68eb28da23f8", 536728149),
-    "attention": ("k_attn.cu", "518b2d720270e27e0cf89e20ac51056b98d2ad0e78eeb124456be25dfc8b4fd9", 185733632),
-    "rowop": ("k_rows.cu", "f029900b35e14e9e8eceee37e8924c2984b9cbe67a086cd03db7f2d1b8f36962", 67837137),
+    "qkv": ("k_gemm.cu", "79ff95039fb8749ceccd1ac0b478dcc5ae5aafe618000a9b9ca91f3b598bbc65", 259947136),
+    "o": ("k_gemm.cu", "79ff95039fb8749ceccd1ac0b478dcc5ae5aafe618000a9b9ca91f3b598bbc65", 187247317),
+    "gateup": ("k_gemm.cu", "79ff95039fb8749ceccd1ac0b478dcc5ae5aafe618000a9b9ca91f3b598bbc65", 345429205),
+    "down": ("k_gemm.cu", "79ff95039fb8749ceccd1ac0b478dcc5ae5aafe618000a9b9ca91f3b598bbc65", 537837141),
+    "attention": ("k_attn.cu", "518b2d720270e27e0cf89e20ac51056b98d2ad0e78eeb124456be25dfc8b4fd9", 187152896),
+    "rowop": ("k_rows.cu", "f029900b35e14e9e8eceee37e8924c2984b9cbe67a086cd03db7f2d1b8f36962", 67805909),
 }
 
 # The workloads whose launches have the captured shapes.
