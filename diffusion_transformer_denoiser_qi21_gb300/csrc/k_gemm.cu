@@ -101,6 +101,10 @@ struct GemmCfg {
   static constexpr int kTailWarpBytes = 48 * 1024;
   static_assert(4 * kTailWarpBytes <= kStages * kStageBytes, "tail staging exceeds the operand ring");
   static_assert(BN * 128 <= kTailWarpBytes, "tail staging of one warp");
+  // epilogue warps: two per TMEM lane quadrant for qkv (one 128-column head
+  // each), one per quadrant otherwise
+  static constexpr int kEpiWarps = (EPI == EPI_QKV || EPI == EPI_QKV_KV) ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kBarBytes = 512;
   static_assert((2 * kStages + 4 + 4 * kXBufs + 32) * 8 + 8 <= kBarBytes, "barrier region");
   static constexpr int kSmem = kEpiOff + kEpiBytes + kBarBytes + 1024;
@@ -288,50 +292,60 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
     for (int hc = o0 / 128; hc < o1 / 128; ++hc) {
       const int col = n0 + hc * 128;
       const int part = col / qe.H;  // 0 q, 1 k, 2 v (uniform over the tile)
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tbase + hc * 128 + c * 32, r[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(r[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) padd.add<2>(r[c], hc * 128 + c * 32);
-      if (!live) continue;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) f8_scale<OP>(r[c], sa, ep.sw, col + c * 32);
       uint16_t* dst = out + col;
       // prefill: the same k / v values into the cache row (K at col - H, V at col - H)
       uint16_t* kvd = (EPI == EPI_QKV_KV && part > 0)
                           ? static_cast<uint16_t*>(qe.kv) + static_cast<size_t>(row) * 2 * qe.H + (col - qe.H)
                           : nullptr;
+      // one 32-column chunk of the head: accumulator (+ the other K parts'
+      // partials, x the FP8 scales) in r
+      auto chunk = [&](int c, uint32_t (&r)[32]) {
+        tmem_ld32(tbase + hc * 128 + c * 32, r);
+        tmem_ld_wait(r);
+        padd.add<2>(r, hc * 128 + c * 32);
+        f8_scale<OP>(r, sa, ep.sw, col + c * 32);
+      };
       if (part == 2) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          chunk(c, r);
+          if (!live) continue;
 #pragma unroll
           for (int j2 = 0; j2 < 2; ++j2) {
             uint32_t v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              v[e] = pack2<BF>(__uint_as_float(r[c][16 * j2 + 2 * e]), __uint_as_float(r[c][16 * j2 + 2 * e + 1]));
+              v[e] = pack2<BF>(__uint_as_float(r[16 * j2 + 2 * e]), __uint_as_float(r[16 * j2 + 2 * e + 1]));
             stg8(dst + c * 32 + j2 * 16, v);
             if constexpr (EPI == EPI_QKV_KV) stg8(kvd + c * 32 + j2 * 16, v);
           }
+        }
         continue;
       }
+      // two passes over the head in TMEM, 32 columns in registers at a
+      // time: the sum of squares, then normalise, rotate and store
       float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        chunk(c, r);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float v = __uint_as_float(r[c][e]);
+          const float v = __uint_as_float(r[e]);
           ss[e & 3] = fmaf(v, v, ss[e & 3]);
         }
+      }
       const float inv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / 128.f) + qe.eps);
       // the norm weights (the caller's, 16-byte aligned; the same address in
       // every lane) in 16-byte loads; the per-row tables and outputs, in
       // the library's 256-byte aligned buffers, 32 bytes at a time
       const float4* w4 = reinterpret_cast<const float4*>(part == 0 ? qe.norm_q : qe.norm_k);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        chunk(c, r);
+        if (!live) continue;
 #pragma unroll
         for (int j2 = 0; j2 < 2; ++j2) {
           // elements 32c + 16j2 .. +15 = pairs 16c + 8j2 .. +7
@@ -346,8 +360,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t tbase, int row, int M, in
           for (int e = 0; e < 8; ++e) {
             const float4 wq = w[e >> 1];
             const float w0 = (e & 1) ? wq.z : wq.x, w1 = (e & 1) ? wq.w : wq.y;
-            const float a = __uint_as_float(r[c][16 * j2 + 2 * e]) * inv * w0;
-            const float b = __uint_as_float(r[c][16 * j2 + 2 * e + 1]) * inv * w1;
+            const float a = __uint_as_float(r[16 * j2 + 2 * e]) * inv * w0;
+            const float b = __uint_as_float(r[16 * j2 + 2 * e + 1]) * inv * w1;
             v[e] = pack2<BF>(a * cv[e] - b * sv[e], a * sv[e] + b * cv[e]);
           }
           stg8(dst + c * 32 + j2 * 16, v);
@@ -452,7 +466,7 @@ __device__ __forceinline__ TileInfo tile_at(int t, int num_mp, int nN, int G, in
 }
 
 template <int BN, int EPI, int OP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmX, int M, int N, int K, int group, int nfull, int num_tiles,
                    EpiArgs ep) {
@@ -488,7 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 8);  // 4 epilogue warps x 2 CTAs
+      mbar_init(&tempty[i], 2 * C::kEpiWarps);  // the epilogue warps of both CTAs
     }
     for (int i = 0; i < 4 * C::kXBufs + 32; ++i) mbar_init(&xbar[i], 1);
     *abort_flag = 0;
@@ -578,7 +592,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;             // TMEM lane quadrant this warp may access
+    const int h = (warp - 2) >> 2;      // qkv: which of the quadrant's two epilogue warps
     int it = 0;
     int xu = 0;  // EPI_RESID: x chunks this warp has staged in its epilogue buffers
     bool eok = true;
@@ -604,7 +619,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const int P = ti.part >= 0 ? ep.parts : 1;
       const int w = max(ti.bn / P, split_own_min<EPI>());
       const int o0 = ti.part >= 0 ? min(ti.part * w, ti.bn) : 0, o1 = min(o0 + w, ti.bn);
-      const bool owner = o1 > o0;
+      // the columns this warp finishes: with two warps per quadrant (qkv),
+      // one head each of a whole tile; of a K-split part's one owned head,
+      // the first warp finishes it while the second hands over the other
+      // columns' partials
+      int f0 = o0, f1 = o1;
+      bool hand_over = true;
+      if constexpr (C::kEpiWarps == 8) {
+        if (ti.part < 0) {
+          f0 = min(o0 + h * 128, o1);
+          f1 = min(f0 + 128, o1);
+        } else if (h == 1) {
+          f1 = f0;
+        } else {
+          hand_over = false;
+        }
+      }
+      const bool owner = f1 > f0;
       // the last item's x chunks (EPI_RESID) sit after the staged partials
       const int xoff = (P - 1) * w * 128;
       const int row0 = (2 * ti.mp + rank) * kBM + q * 32;  // this warp's first row
@@ -621,18 +652,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const size_t slab = static_cast<size_t>(BN) * 32;
         const size_t sbase = static_cast<size_t>(ti.tail) * P * 8 + rank * 4 + q;  // + 8 per part
         float* mine = ep.part + (sbase + ti.part * 8) * slab + lane;
+        if (hand_over) {
 #pragma unroll 1
-        for (int c = 0; c < ti.bn / 32; ++c) {
-          if (c * 32 >= o0 && c * 32 < o1) continue;
-          uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          tmem_ld_wait(r);
+          for (int c = 0; c < ti.bn / 32; ++c) {
+            if (c * 32 >= o0 && c * 32 < o1) continue;
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            tmem_ld_wait(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) __stcg(mine + static_cast<size_t>(c * 32 + e) * 32, __uint_as_float(r[e]));
+            for (int e = 0; e < 32; ++e) __stcg(mine + static_cast<size_t>(c * 32 + e) * 32, __uint_as_float(r[e]));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) set_flag_release(ep.flags + sbase + ti.part * 8, ep.epoch);
         }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) set_flag_release(ep.flags + sbase + ti.part * 8, ep.epoch);
         bool got = last;  // the schedule guarantees it; anything else is refused, not raced
         if (!last && lane == 0) {
           *abort_flag = 1;
@@ -741,7 +774,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         if (!last) xu += c1 - c0;
       } else {
-        gemm_epilogue<BN, EPI, OP>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, o0, o1, ep, psum);
+        gemm_epilogue<BN, EPI, OP>(tbase, (2 * ti.mp + rank) * kBM + q * 32 + lane, M, ti.n0, f0, f1, ep, psum);
       }
       tc_fence_before();
       __syncwarp();
@@ -902,7 +935,7 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
     if (r.e != cudaSuccess) return r;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * sm_count(), 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     int n = 0;
     r.e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, OP>, &cfg);
@@ -938,7 +971,7 @@ static cudaError_t launch_t(const GemmPlan& p, cudaStream_t s) {
   const int clusters = std::min(total, max_clusters);
   const int group = raster_group(num_mp, p.K, OP == kOpF8 ? 1 : 2);
   EpiArgs ep{p.out, p.ldo, p.gate, p.qkv, p.sa, p.sw, static_cast<float*>(p.part), p.flags, parts, p.epoch};
-  gemm_tc_kernel<BN, EPI, OP><<<2 * clusters, 192, C::kSmem, s>>>(p.tmA, p.tmB, p.tmX, p.M, p.N, p.K, group, nfull,
+  gemm_tc_kernel<BN, EPI, OP><<<2 * clusters, C::kThreads, C::kSmem, s>>>(p.tmA, p.tmB, p.tmX, p.M, p.N, p.K, group, nfull,
                                                                   total, ep);
   return cudaGetLastError();
 }
