@@ -30,7 +30,7 @@
 // the B tile in its shared memory, and receives rows [128 r, 128 r + 128)
 // of the accumulator in its TMEM. Each SM therefore holds only half of B:
 // 32 KB stages instead of 48 KB, six of them, enough operand data in flight
-// to cover the TMA latency. 6 warps per CTA:
+// to cover the TMA latency. 6 warps per CTA (10 for qkv):
 //   warp 0     TMA producer (both CTAs): A 128x64 and B (BN/2)x64 tiles
 //              (128-byte swizzle) into a 6-stage ring; the loads of both CTAs
 //              complete on the even CTA's "full" mbarrier
@@ -40,7 +40,9 @@
 //   warps 2-5  epilogue (both CTAs): tcgen05.ld of their 32-lane quadrant,
 //              fused op, 128-bit stores; two TMEM accumulators so the
 //              epilogue of tile i overlaps the MMAs of tile i+1; each warp
-//              reports "accumulator free" to the even CTA.
+//              reports "accumulator free" to the even CTA. The qkv
+//              instances have two epilogue warps per quadrant (warps 2-9),
+//              one 128-column head each.
 // Schedule (tile_at): tiles in groups of G pair rows (column blocks outer,
 // the pair rows of a group inner), G chosen on the host so that the group's
 // A rows stay in L2 while its column blocks stream past; whole tiles of odd
