@@ -139,6 +139,11 @@ WORKLOADS = {
     "cfg_pair_d256": Workload("cfg_pair_d256", 256, 2, 768, 2, ((_t(18),), (_t(1),)), (9, 15)),
     # smallest target: one row, one-row prefix
     "single_row_d256": Workload("single_row_d256", 256, 2, 768, 1, ((_t(1),),), (1, 1)),
+    # an odd head count (3 heads, dim 384): the qkv and O projections have
+    # N = 1152 and 384, not multiples of 256, so they run 128-column tiles;
+    # 4356 target rows make the qkv's last wave a partial one (162 tile
+    # pairs on 76 clusters), split along K
+    "heads3_d384_n4356": Workload("heads3_d384_n4356", 384, 3, 1024, 2, ((_t(18),),), (66, 66)),
     # one full-width block with the 4114-row condition prefix: every launch
     # has the shapes of one layer of step32_cond4114_n4096 (small profiling
     # captures of those kernels)

@@ -38,7 +38,8 @@ def _teacher_forced_layer(run, layer, s, W, cfg, rows_pre=None, rows_step=None):
     return teacher_forced_layer(run, layer, s, W, cfg, TOL, rows_pre=rows_pre, rows_step=rows_step)
 
 
-SMALL = ["tiny_block_d256", "chain32_d256_mixed", "ragged_d512", "cfg_pair_d256", "single_row_d256"]
+SMALL = ["tiny_block_d256", "chain32_d256_mixed", "ragged_d512", "cfg_pair_d256", "single_row_d256",
+         "heads3_d384_n4356"]
 
 
 @pytest.mark.parametrize("name", SMALL)
