@@ -51,6 +51,34 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   return ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
 }
 
+// Two f32 lanes in one 64-bit register pair and packed f32x2 arithmetic on
+// them (one instruction for both lanes).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f32x2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // resident CTAs per SM: four, two for the widest rows (register budget)
 constexpr int rowop_ctas_per_sm(int nv) { return nv >= 8 ? 2 : 4; }
 
@@ -94,29 +122,42 @@ __global__ void __launch_bounds__(kRowThreads, rowop_ctas_per_sm(NV))
       }
     }
     if (xn != nullptr) {
-      float sm = 0.f;
+      // the row's values as pairs of lanes (x, y), (z, w) of each float4,
+      // the arithmetic packed two lanes an instruction
+      uint64_t s2 = 0ull;
 #pragma unroll
       for (int j = 0; j < NV; ++j)
-        if (threadIdx.x + j * kRowThreads < nv) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-      const float mean = block_sum_256(sm, red) / static_cast<float>(dim);
-      float sq = 0.f;
+        if (threadIdx.x + j * kRowThreads < nv)
+          s2 = add_x2(s2, add_x2(f32x2(v[j].x, v[j].y), f32x2(v[j].z, v[j].w)));
+      const float2 sp = f32x2_split(s2);
+      const float mean = block_sum_256(sp.x + sp.y, red) / static_cast<float>(dim);
+      const uint64_t nm2 = f32x2(-mean, -mean);
+      uint64_t q2 = 0ull;
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         if (threadIdx.x + j * kRowThreads < nv) {
-          const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
-          sq += (a * a + b * b) + (c * c + d * d);
+          const uint64_t a = add_x2(f32x2(v[j].x, v[j].y), nm2), b = add_x2(f32x2(v[j].z, v[j].w), nm2);
+          q2 = fma_x2(a, a, q2);
+          q2 = fma_x2(b, b, q2);
         }
       }
-      const float inv = rsqrtf(block_sum_256(sq, red) / static_cast<float>(dim) + eps);
+      const float2 qp = f32x2_split(q2);
+      const float inv = rsqrtf(block_sum_256(qp.x + qp.y, red) / static_cast<float>(dim) + eps);
+      const uint64_t one2 = f32x2(1.f, 1.f), inv2 = f32x2(inv, inv);
       uint2* o2 = reinterpret_cast<uint2*>(xn + static_cast<size_t>(row) * dim);
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int idx = threadIdx.x + j * kRowThreads;
         if (idx < nv) {
           const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + idx);
+          // (v - mean) inv (1 + scale)
+          const float2 lo = f32x2_split(
+              mul_x2(mul_x2(add_x2(f32x2(v[j].x, v[j].y), nm2), inv2), add_x2(f32x2(sc.x, sc.y), one2)));
+          const float2 hi = f32x2_split(
+              mul_x2(mul_x2(add_x2(f32x2(v[j].z, v[j].w), nm2), inv2), add_x2(f32x2(sc.z, sc.w), one2)));
           uint2 out;
-          out.x = pack2<BF>((v[j].x - mean) * inv * (1.f + sc.x), (v[j].y - mean) * inv * (1.f + sc.y));
-          out.y = pack2<BF>((v[j].z - mean) * inv * (1.f + sc.z), (v[j].w - mean) * inv * (1.f + sc.w));
+          out.x = pack2<BF>(lo.x, lo.y);
+          out.y = pack2<BF>(hi.x, hi.y);
           o2[idx] = out;
         }
       }
